@@ -1,0 +1,332 @@
+"""Pins of the fp64 oracle against things other than itself (CPU only).
+
+- a hand-worked example (tests/golden/gated_delta_hand.json, exact decimals derived by hand);
+- brute force: S_T = S_0 M_1..M_T + sum_t beta_t v_t k_t^T M_{t+1}..M_T with
+  M_t = diag(alpha_t)(I - beta_t k_t k_t^T), as explicit dense matrix products;
+- closed forms and special cases of the gated delta rule;
+- conv1d against numpy.convolve and scipy's logistic function; L2 norm against numpy.linalg;
+- invariants: batched == per stream, split call with carried state == one call, GQA mapping,
+  thread-count independence, and the chunked (WY) restatement == token by token.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+from tests.chunk_algebra import chunked_unit
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "gated_delta_hand.json")
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+def rand_unit_inputs(r, T, dk, dv, per_channel, Hk=1, Hv=1):
+    q = r.standard_normal((T, Hk, dk)) / np.sqrt(dk)
+    k = r.standard_normal((T, Hk, dk)) / np.sqrt(dk)
+    v = r.standard_normal((T, Hv, dv)) * 0.5
+    g = -np.log1p(np.exp(r.standard_normal((T, Hv, dk) if per_channel else (T, Hv))))
+    beta = expit(r.standard_normal((T, Hv)))
+    return q, k, v, g, beta
+
+
+def run_oracle(h, q, k, v, g, beta, lengths, scale, per_channel, threads=None):
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    return oracle.gated_delta(h, q, k, v, g, beta, cu, scale=scale, per_channel=per_channel,
+                              threads=threads)
+
+
+# ---------------------------------------------------------------- hand-worked golden example
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_golden_hand_example(variant):
+    G = json.load(open(GOLDEN))[variant]
+    S0 = np.array(G["S0"], dtype=float)
+    k = np.array(G["k"], dtype=float)[:, None, :]
+    q = np.array(G["q"], dtype=float)[:, None, :]
+    v = np.array(G["v"], dtype=float)[:, None, :]
+    T = k.shape[0]
+    g = np.array(G["g"], dtype=float).reshape(T, 1, -1) if variant == "kda" else \
+        np.array(G["g"], dtype=float).reshape(T, 1)
+    beta = np.array(G["beta"], dtype=float).reshape(T, 1)
+    h = S0.T[None, None]  # H = S^T, [B][Hv][dk][dv]
+    out, h1 = run_oracle(h, q, k, v, g, beta, [T], 1.0, variant == "kda")
+    np.testing.assert_allclose(out[:, 0, :], np.array(G["o"]), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(h1[0, 0].T, np.array(G["S_final"]), rtol=1e-13, atol=1e-13)
+
+
+def test_golden_hand_conv():
+    G = json.load(open(GOLDEN))["conv"]
+    out, st = oracle.conv1d_silu(np.array(G["state"]), np.array(G["x"]), np.array(G["w"]))
+    y = np.array(G["y_pre_silu"], dtype=float)
+    np.testing.assert_allclose(out, y * expit(y), rtol=1e-15)
+    np.testing.assert_array_equal(st, np.array(G["new_state"]))
+
+
+# ---------------------------------------------------------------- brute force
+def brute_unit(S0, q, k, v, g, beta, scale):
+    """Outputs and final S of one unit from explicit products of transition matrices."""
+    T, dk = k.shape
+    I = np.eye(dk)
+
+    def M(t):
+        a = np.exp(g[t]) * np.ones(dk)
+        return np.diag(a) @ (I - beta[t] * np.outer(k[t], k[t]))
+
+    outs = []
+    for t in range(T):
+        prod = I.copy()
+        for s in range(t + 1):
+            prod = prod @ M(s)
+        St = S0 @ prod
+        for s in range(t + 1):
+            tail = I.copy()
+            for r_ in range(s + 1, t + 1):
+                tail = tail @ M(r_)
+            St = St + beta[s] * np.outer(v[s], k[s]) @ tail
+        outs.append(scale * St @ q[t])
+    return np.array(outs), St
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("T,dk,dv", [(1, 2, 3), (5, 4, 4), (6, 3, 2)])
+def test_brute_force_products(per_channel, T, dk, dv):
+    r = rng(T * 100 + dk * 10 + dv + per_channel)
+    q, k, v, g, beta = rand_unit_inputs(r, T, dk, dv, per_channel)
+    S0 = r.standard_normal((dv, dk)) * 0.3
+    out, h1 = run_oracle(S0.T[None, None], q, k, v, g, beta, [T], 0.7, per_channel)
+    gg = g[:, 0] if per_channel else g[:, 0]
+    ob, Sb = brute_unit(S0, q[:, 0], k[:, 0], v[:, 0], gg, beta[:, 0], 0.7)
+    np.testing.assert_allclose(out[:, 0], ob, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h1[0, 0].T, Sb, rtol=1e-12, atol=1e-12)
+
+
+def test_brute_force_gqa_multistream():
+    """Two streams, Hk=1 shared by Hv=2 v-heads: each (stream, v-head) equals its brute force."""
+    r = rng(7)
+    lengths = [3, 4]
+    T = sum(lengths)
+    q, k, v, g, beta = rand_unit_inputs(r, T, 3, 2, True, Hk=1, Hv=2)
+    S0 = r.standard_normal((2, 2, 2, 3)) * 0.3  # [B][Hv][dv][dk]
+    out, h1 = run_oracle(np.transpose(S0, (0, 1, 3, 2)), q, k, v, g, beta, lengths, 1.0, True)
+    off = 0
+    for s, L in enumerate(lengths):
+        sl = slice(off, off + L)
+        for j in range(2):
+            ob, Sb = brute_unit(S0[s, j], q[sl, 0], k[sl, 0], v[sl, j], g[sl, j], beta[sl, j], 1.0)
+            np.testing.assert_allclose(out[sl, j], ob, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(h1[s, j].T, Sb, rtol=1e-12, atol=1e-12)
+        off += L
+
+
+# ---------------------------------------------------------------- closed forms
+def test_beta_zero_pure_decay():
+    r = rng(1)
+    T, d = 7, 4
+    q, k, v, g, beta = rand_unit_inputs(r, T, d, d, True)
+    beta[:] = 0.0
+    S0 = r.standard_normal((d, d))
+    out, h1 = run_oracle(S0.T[None, None], q, k, v, g, beta, [T], 0.5, True)
+    cum = np.cumsum(g[:, 0, :], axis=0)
+    for t in range(T):
+        np.testing.assert_allclose(out[t, 0], 0.5 * S0 @ (np.exp(cum[t]) * q[t, 0]), rtol=1e-13)
+    np.testing.assert_allclose(h1[0, 0].T, S0 * np.exp(cum[-1])[None, :], rtol=1e-13)
+
+
+def test_delta_write_is_exact():
+    """beta = 1 and |k| = 1: after each step S_t k_t = v_t (read with q = k, scale 1)."""
+    r = rng(2)
+    T, d = 9, 5
+    k = r.standard_normal((T, 1, d))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = r.standard_normal((T, 1, d))
+    g = -np.abs(r.standard_normal((T, 1)))
+    beta = np.ones((T, 1))
+    out, _ = run_oracle(r.standard_normal((1, 1, d, d)), k, k, v, g, beta, [T], 1.0, False)
+    np.testing.assert_allclose(out[:, 0], v[:, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_single_token_from_zero_state():
+    r = rng(3)
+    d = 6
+    q, k, v, g, beta = rand_unit_inputs(r, 1, d, d, False)
+    out, _ = run_oracle(np.zeros((1, 1, d, d)), q, k, v, g, beta, [1], 0.25, False)
+    expect = 0.25 * beta[0, 0] * (k[0, 0] @ q[0, 0]) * v[0, 0]
+    np.testing.assert_allclose(out[0, 0], expect, rtol=1e-14, atol=1e-16)
+
+
+def test_orthonormal_keys_no_decay():
+    """alpha = 1, beta = 1, orthonormal keys: S_T = S_0 (I - sum k k^T) + sum v k^T."""
+    r = rng(4)
+    d, T = 6, 4
+    Qm, _ = np.linalg.qr(r.standard_normal((d, d)))
+    k = Qm[:, :T].T[:, None, :]
+    v = r.standard_normal((T, 1, d))
+    S0 = r.standard_normal((d, d))
+    _, h1 = run_oracle(S0.T[None, None], k, k, v, np.zeros((T, 1)), np.ones((T, 1)), [T], 1.0,
+                       False)
+    kk = sum(np.outer(k[t, 0], k[t, 0]) for t in range(T))
+    vk = sum(np.outer(v[t, 0], k[t, 0]) for t in range(T))
+    np.testing.assert_allclose(h1[0, 0].T, S0 @ (np.eye(d) - kk) + vk, rtol=1e-12, atol=1e-12)
+
+
+def test_kda_with_broadcast_gate_equals_gdn():
+    r = rng(5)
+    T, d = 11, 4
+    q, k, v, g, beta = rand_unit_inputs(r, T, d, d, False)
+    h0 = r.standard_normal((1, 1, d, d))
+    o1, h1 = run_oracle(h0, q, k, v, g, beta, [T], 0.3, False)
+    o2, h2 = run_oracle(h0, q, k, v, np.repeat(g[:, :, None], d, axis=2), beta, [T], 0.3, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(h1, h2)
+
+
+# ---------------------------------------------------------------- conv and L2
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+@pytest.mark.parametrize("t", [1, 2, 5, 17])
+def test_conv_matches_numpy_convolve(K, t):
+    r = rng(K * 31 + t)
+    C = 5
+    state = r.standard_normal((K - 1, C))
+    x = r.standard_normal((t, C))
+    w = r.standard_normal((C, K))
+    b = r.standard_normal(C)
+    out, st = oracle.conv1d_silu(state, x, w, b)
+    xh = np.concatenate([state, x], axis=0)
+    for c in range(C):
+        y = np.convolve(xh[:, c], w[c, ::-1], mode="valid") + b[c]
+        np.testing.assert_allclose(out[:, c], y * expit(y), rtol=1e-13, atol=1e-15)
+    np.testing.assert_array_equal(st, xh[t:t + K - 1])
+
+
+def test_conv_special_taps():
+    r = rng(9)
+    x = r.standard_normal((6, 3))
+    w1 = r.standard_normal((3, 1))
+    out, _ = oracle.conv1d_silu(np.zeros((0, 3)), x, w1)
+    y = x * w1[:, 0]
+    np.testing.assert_allclose(out, y * expit(y), rtol=1e-14)
+    w = np.zeros((3, 4))
+    w[:, 3] = 1.0  # e_{K-1}: the current token only
+    out, _ = oracle.conv1d_silu(r.standard_normal((3, 3)), x, w)
+    np.testing.assert_allclose(out, x * expit(x), rtol=1e-14)
+
+
+def test_conv_varlen_short_streams_carry_state():
+    """Streams shorter than kernel-1 keep part of the old state, in order."""
+    r = rng(10)
+    C, K = 2, 4
+    lengths = [1, 0, 2, 5]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    x = r.standard_normal((cu[-1], C))
+    states = r.standard_normal((len(lengths), K - 1, C))
+    w = r.standard_normal((C, K))
+    _, ns = oracle.conv1d_silu_varlen(states, x, w, cu)
+    for s, L in enumerate(lengths):
+        xh = np.concatenate([states[s], x[cu[s]:cu[s + 1]]])
+        np.testing.assert_array_equal(ns[s], xh[L:L + K - 1])
+
+
+def test_l2norm_properties():
+    r = rng(11)
+    t, H, d = 5, 3, 8
+    x = r.standard_normal((t, H * d + 4))
+    x[2, d:2 * d] = 0.0
+    eps = 1e-6
+    y = oracle.l2norm_heads(x, H, d, eps)
+    for h in range(H):
+        xs, ys = x[:, h * d:(h + 1) * d], y[:, h * d:(h + 1) * d]
+        nx = np.linalg.norm(xs, axis=1)
+        np.testing.assert_allclose(np.linalg.norm(ys, axis=1), nx / np.sqrt(nx ** 2 + eps),
+                                   rtol=1e-14)
+        nz = nx > 0
+        np.testing.assert_allclose(ys[nz] * nx[nz, None], xs[nz] * np.linalg.norm(ys[nz], axis=1)[:, None],
+                                   rtol=1e-13, atol=1e-15)
+    assert np.all(y[2, d:2 * d] == 0.0)
+    np.testing.assert_array_equal(y[:, H * d:], x[:, H * d:])  # channels past the heads untouched
+
+
+# ---------------------------------------------------------------- invariants
+def test_batched_equals_per_stream_bitwise():
+    r = rng(12)
+    lengths = [5, 9, 1, 7]
+    T = sum(lengths)
+    q, k, v, g, beta = rand_unit_inputs(r, T, 4, 3, True, Hk=2, Hv=4)
+    h0 = r.standard_normal((4, 4, 4, 3))
+    out, h1 = run_oracle(h0, q, k, v, g, beta, lengths, 0.5, True)
+    off = 0
+    for s, L in enumerate(lengths):
+        sl = slice(off, off + L)
+        o_s, h_s = run_oracle(h0[s:s + 1], q[sl], k[sl], v[sl], g[sl], beta[sl], [L], 0.5, True)
+        np.testing.assert_array_equal(out[sl], o_s)
+        np.testing.assert_array_equal(h1[s], h_s[0])
+        off += L
+
+
+def test_split_call_equals_single_call_bitwise():
+    r = rng(13)
+    T, cut = 23, 10
+    q, k, v, g, beta = rand_unit_inputs(r, T, 4, 4, False, Hk=1, Hv=2)
+    h0 = r.standard_normal((1, 2, 4, 4))
+    o_all, h_all = run_oracle(h0, q, k, v, g, beta, [T], 0.5, False)
+    a, b = slice(0, cut), slice(cut, T)
+    o_a, h_a = run_oracle(h0, q[a], k[a], v[a], g[a], beta[a], [cut], 0.5, False)
+    o_b, h_b = run_oracle(h_a, q[b], k[b], v[b], g[b], beta[b], [T - cut], 0.5, False)
+    np.testing.assert_array_equal(o_all, np.concatenate([o_a, o_b]))
+    np.testing.assert_array_equal(h_all, h_b)
+    # conv state carried across the split as well
+    x = r.standard_normal((T, 6))
+    w = r.standard_normal((6, 4))
+    st0 = r.standard_normal((3, 6))
+    out_all, st_all = oracle.conv1d_silu(st0, x, w)
+    out_a, st_a = oracle.conv1d_silu(st0, x[:cut], w)
+    out_b, st_b = oracle.conv1d_silu(st_a, x[cut:], w)
+    np.testing.assert_array_equal(out_all, np.concatenate([out_a, out_b]))
+    np.testing.assert_array_equal(st_all, st_b)
+
+
+def test_thread_count_independent():
+    r = rng(14)
+    lengths = [13, 4, 20]
+    q, k, v, g, beta = rand_unit_inputs(r, sum(lengths), 4, 4, True, Hk=1, Hv=3)
+    h0 = r.standard_normal((3, 3, 4, 4))
+    o1, h1 = run_oracle(h0, q, k, v, g, beta, lengths, 0.5, True, threads=1)
+    o2, h2 = run_oracle(h0, q, k, v, g, beta, lengths, 0.5, True, threads=5)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(h1, h2)
+
+
+def test_zero_length_stream_is_noop():
+    r = rng(15)
+    lengths = [3, 0, 2]
+    q, k, v, g, beta = rand_unit_inputs(r, 5, 4, 4, False)
+    h0 = r.standard_normal((3, 1, 4, 4))
+    _, h1 = run_oracle(h0, q, k, v, g, beta, lengths, 1.0, False)
+    np.testing.assert_array_equal(h1[1], h0[1])
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("T,C", [(1, 64), (63, 64), (64, 64), (150, 64), (37, 8), (100, 16)])
+def test_chunked_restatement_equals_token_by_token(per_channel, T, C):
+    r = rng(T + C + per_channel)
+    d = 8
+    q, k, v, g, beta = rand_unit_inputs(r, T, d, d, per_channel)
+    h0 = r.standard_normal((1, 1, d, d)) * 0.1
+    out, h1 = run_oracle(h0, q, k, v, g, beta, [T], 0.4, per_channel)
+    oc, hc = chunked_unit(h0[0, 0], q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0],
+                          scale=0.4, C=C)
+    np.testing.assert_allclose(oc, out[:, 0], rtol=1e-10, atol=1e-10)
+    np.testing.assert_allclose(hc, h1[0, 0], rtol=1e-10, atol=1e-10)
+
+
+def test_planted_mistake_is_caught():
+    """A dropped decay (alpha forced to 1) in the oracle's input is visible to the brute force."""
+    r = rng(16)
+    q, k, v, g, beta = rand_unit_inputs(r, 4, 3, 3, False)
+    S0 = r.standard_normal((3, 3))
+    out, _ = run_oracle(S0.T[None, None], q, k, v, np.zeros_like(g), beta, [4], 1.0, False)
+    ob, _ = brute_unit(S0, q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], 1.0)
+    assert np.max(np.abs(out[:, 0] - ob)) > 1e-3
