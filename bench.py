@@ -1,0 +1,404 @@
+#!/usr/bin/env python3
+"""Benchmark of the chunked GDN/KDA prefill hot path on GB300.
+
+One step = one pass of the whole hot path over one packed batch that is already resident in
+HBM: conv1d + SiLU (carried conv state) -> L2 over the q|k heads -> chunked gated delta rule,
+all through the C ABI. Default workload: GDN batched, 8 streams x 2048 tokens, 16 heads,
+head dim 128, bf16 activations, fp32 states.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the fp64 CPU oracle instead (the
+reference arm of this path), on bounded samples of the same workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+Multi-GPU (replicas, weak scaling): torchrun --nproc-per-node N bench.py --gpus N ...
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from linear_attention_chunked_conv1d_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "gdn_batched_8x2048_h16_d128"
+METRIC = "prefill tokens/s per GDN/KDA layer"
+CHUNK = 64
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------------------ accounting
+def act_bytes(wl) -> int:
+    return 2 if wl.dtype == "bf16" else 4
+
+
+def path_algorithmic(wl, lengths):
+    """Algorithmic bytes and FLOPs of one pass of the (fused) path: x read once, gates, output,
+    states read + written, conv weights. FLOPs per token and v-head: 2C dk (K K^T, Q K^T lower
+    triangles) + C (dk + dv) (forward substitution) + C dv (P U') + 6 dk dv (w H, Q H, K^T U')."""
+    s = act_bytes(wl)
+    T = sum(lengths)
+    d, K = wl.d, wl.conv_kernel
+    gate = 4 * wl.Hv * (d if wl.variant == "kda" else 1)
+    per_tok = wl.cd * s + gate + 4 * wl.Hv + wl.Hv * d * s
+    per_stream = 2 * 4 * wl.Hv * d * d + 2 * s * (K - 1) * wl.cd
+    B = per_tok * T + per_stream * len(lengths) + wl.cd * K * s
+    F = T * wl.Hv * (2 * CHUNK * d + CHUNK * 2 * d + CHUNK * d + 6 * d * d)
+    return B, F
+
+
+def kernel_algorithmic_bytes(wl, lengths):
+    """Algorithmic bytes per launch of each kernel of the (unfused) path."""
+    s = act_bytes(wl)
+    T, d, K = sum(lengths), wl.d, wl.conv_kernel
+    B = len(lengths)
+    conv = 2 * T * wl.cd * s + wl.cd * K * s + 2 * B * (K - 1) * wl.cd * s
+    l2 = 2 * T * 2 * wl.Hk * d * s
+    gate = 4 * wl.Hv * (d if wl.variant == "kda" else 1)
+    rec = (T * (2 * wl.Hk * d * s + wl.Hv * d * s + gate + 4 * wl.Hv + wl.Hv * d * s)
+           + 2 * B * wl.Hv * d * d * 4)
+    return {"conv1d_silu": conv, "l2norm_heads": l2, "recurrence": rec}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha(name: str) -> str:
+    src = os.path.join(ROOT, "linear_attention_chunked_conv1d_gb300", "csrc", name)
+    with open(src, "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes (read + write) per launch from profiles/traffic.txt, only if the kernel source
+    is unchanged since the counters were taken (lines: file workload sha12 bytes)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    sha = kernel_source_sha(kernel_file)
+    for line in open(p):
+        parts = line.split()
+        if len(parts) == 4 and parts[0] == kernel_file and parts[1] == workload and parts[2] == sha:
+            return int(parts[3])
+    return None
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def oracle_sample(wl, inputs_cpu_stream, threads):
+    """The oracle (as it stands) over one stream: front end + recurrence, all heads."""
+    import oracle
+    x, conv_state, h, g, beta, L, conv_w = inputs_cpu_stream
+    cu = np.array([0, L])
+    q, k, v, _ = oracle.front_end(x, conv_w, conv_state[None], cu, Hk=wl.Hk,
+                                  Hv=wl.Hv, dk=wl.d, dv=wl.d, eps=1e-6, act_dtype=wl.dtype)
+    oracle.gated_delta(h[None], q, k, v, g, beta, cu.astype(np.int32),
+                       scale=1.0 / math.sqrt(wl.d), per_channel=wl.variant == "kda",
+                       threads=threads)
+
+
+def stream_cpu(inp, s, conv_w):
+    cu = np.concatenate([[0], np.cumsum(inp["lengths"])])
+    a, b = int(cu[s]), int(cu[s + 1])
+    f = lambda t: t.detach().to("cpu", torch.float64).numpy()  # noqa: E731
+    return (f(inp["x"][a:b]), f(inp["conv_state"][s]), f(inp["h"][s]), f(inp["g"][a:b]),
+            f(inp["beta"][a:b]), b - a, conv_w)
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """Time the oracle on whole streams of the workload until about budget_s of CPU work."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    conv_w = inp["conv_w"].detach().to("cpu", torch.float64).numpy()
+    done_tokens, elapsed, streams = 0, 0.0, 0
+    order = list(range(wl.B))
+    for s in order:
+        data = stream_cpu(inp, s, conv_w)
+        t0 = time.perf_counter()
+        oracle_sample(wl, data, threads)
+        elapsed += time.perf_counter() - t0
+        done_tokens += data[5]
+        streams += 1
+        if elapsed >= budget_s:
+            break
+    return {"value": done_tokens / elapsed, "unit": "tokens/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{streams} of {wl.B} streams ({done_tokens} tokens, all {wl.Hv} v-heads): "
+                      f"fp64 conv1d+SiLU -> L2 -> token-by-token recurrence, {elapsed:.1f} s"}
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = make_inputs(wl, device="cpu", seed=0)
+    conv_w = inp["conv_w"].to(torch.float64).numpy()
+    threads = os.cpu_count() or 1
+    # each step: the oracle over one whole stream (all v-heads), cycling through the streams
+    data = [stream_cpu(inp, s, conv_w) for s in range(min(wl.B, 2))]
+    for i in range(args.warmup):
+        oracle_sample(wl, data[i % len(data)], threads)
+    times, toks = [], 0
+    for i in range(args.steps):
+        d = data[i % len(data)]
+        t0 = time.perf_counter()
+        oracle_sample(wl, d, threads)
+        times.append(time.perf_counter() - t0)
+        toks += d[5]
+    total = sum(times)
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe in DESIGN.md)",
+        "config": {"workload": wl.name, "streams": wl.B, "Hk": wl.Hk, "Hv": wl.Hv,
+                   "head_dim": wl.d, "variant": wl.variant, "activations": wl.dtype},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: one whole stream ({data[0][5]} tokens, all "
+                                   f"{wl.Hv} v-heads) of the workload, fp64 front end + "
+                                   "token-by-token recurrence"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import linear_attention_chunked_conv1d_gb300 as la
+    from linear_attention_chunked_conv1d_gb300.path import PrefillPass
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    la._load()
+    inp = make_inputs(wl, device=dev, seed=rank)  # each replica its own batch (weak scaling)
+    lengths = inp["lengths"]
+    T = sum(lengths)
+    p = PrefillPass(wl, inp)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        p.run()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        ev[i][0].record(stream)
+        p.front_end()
+        ev[i][1].record(stream)
+        p.recurrence()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    front_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    rec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms = sum(step_ms) / len(step_ms)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API: pinned host inputs in, result out, every step
+    x_h = inp["x"].cpu().pin_memory()
+    g_h = inp["g"].cpu().pin_memory()
+    b_h = inp["beta"].cpu().pin_memory()
+    out_h = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (x_h, g_h, b_h))
+    d2h = out_h.numel() * out_h.element_size()
+    for _ in range(2):
+        inp["x"].copy_(x_h, non_blocking=True)
+        p.run()
+        out_h.copy_(p.out, non_blocking=True)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        inp["x"].copy_(x_h, non_blocking=True)
+        inp["g"].copy_(g_h, non_blocking=True)
+        inp["beta"].copy_(b_h, non_blocking=True)
+        p.run()
+        out_h.copy_(p.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    kb = kernel_algorithmic_bytes(wl, lengths)
+    rec_avg = sum(rec_ms) / len(rec_ms)
+    front_avg = sum(front_ms) / len(front_ms)
+    rec_achieved = kb["recurrence"] / (rec_avg * 1e-3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    B_alg, F_alg = path_algorithmic(wl, lengths)
+    t_roof = max(F_alg / (float(peaks["bf16_tflops"]) * 1e12), B_alg / (hbm * 1e9))
+    kernel_file = "chunk_simt.cu"
+    traffic = profiled_traffic(kernel_file, wl.name)
+    tokens_all = T * world
+    line = {
+        "metric": METRIC,
+        "value": tokens_all / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; x~N(0,1), conv w~N(0,0.25), h~N(0,0.02), "
+                "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
+        "config": {"workload": wl.name, "streams": wl.B, "tokens_per_step": T,
+                   "Hk": wl.Hk, "Hv": wl.Hv, "head_dim": wl.d, "variant": wl.variant,
+                   "activations": wl.dtype, "states": "f32", "chunk": CHUNK,
+                   "l2": "flushed between timed steps (write of a 258 MiB buffer)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "hbm", "kernel": "chunk_simt_kernel (recurrence)",
+                     "achieved": rec_achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": rec_achieved / hbm, "traffic": traffic,
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": kb["recurrence"],
+                     "avg_launch_ms": rec_avg},
+        "phases_ms": {"front_end(conv1d+silu, l2)": front_avg, "recurrence": rec_avg},
+        "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms * 1e-3),
+                          "bytes_alg": B_alg, "flops_alg": F_alg,
+                          "peaks": f"{peak_src}: {hbm} GB/s, {peaks['bf16_tflops']} TFLOP/s bf16"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * linattn — C ABI of the GB300 (sm_103a) chunked gated-delta-rule prefill library.
+ *
+ * The path (metrale engine documentation pages "split_prefill.rs", trait
+ * LayerSplitPrefill, and "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill):
+ *
+ *   x --conv1d+SiLU (carried conv state)--> [q | k | v] --L2 per q|k head--> gated delta rule
+ *   S_t = S_{t-1} diag(alpha_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,  o_t = scale S_t q_t,
+ *   alpha_t = exp(g_t) (scalar per v-head: GDN; one value per k-channel: KDA),
+ *
+ * evaluated chunk by chunk (64 tokens) with the WY form: per chunk the cumulative gate gc,
+ * A = strictly-lower(diag(beta) (K K^T (.) decay)), U' = (I + A)^{-1} (diag(beta) V -
+ * diag(beta) (K (.) e^gc) H), O = scale ((Q (.) e^gc) H + P U'), and the carried state
+ * H <- diag(e^gc_L) H + (K (.) e^{gc_L - gc})^T U'.
+ *
+ * Conventions shared by every call
+ *  - Pointers are raw DEVICE pointers owned by the caller, unless stated otherwise. The library
+ *    allocates no device memory and keeps no per-call state; all work is enqueued on `stream`
+ *    (a cudaStream_t passed as uint64_t; 0 = legacy default stream) and is asynchronous.
+ *  - Every check runs on the host BEFORE any launch; on error nothing is launched and no buffer
+ *    is touched. Return value: LA_OK or one of the LA_ERR_* codes; la_last_error() then gives a
+ *    thread-local message.
+ *  - dtype selects the activation type (x, conv weights/state, q, k, v, out): LA_F32 or LA_BF16.
+ *    Gates g, beta and the recurrent state are always fp32.
+ *  - Vector access: every activation pointer must be 16-byte aligned and every activation row
+ *    stride / channel count a multiple of 16 bytes (8 bf16 or 4 fp32 elements).
+ *  - Token counts: a call covers 1..max_tokens tokens; 0 or more than max_tokens is refused with
+ *    LA_ERR_COUNT before any launch ("glm5next_kda/prefill.rs", module invariant and the
+ *    t == 0 || t > ws.max_tokens check of prefill_with_pad_fill).
+ *  - States are updated in place: the conv state and the recurrent state carry a stream from one
+ *    call to the next ("split_prefill.rs", prefill_phase1_conv1d_one advancing the conv state;
+ *    "glm5next_kda/prefill.rs", prefill starting from the carried state).
+ *  - Varlen streams: cu_seqlens is a DEVICE int32 array of B+1 token offsets, cu_seqlens[0] = 0,
+ *    nondecreasing, cu_seqlens[B] = total_tokens, each length <= max_seqlen. A zero-length
+ *    stream is a no-op for its state. The kernels check these bounds on the device; a violation
+ *    skips the offending stream and raises a flag that la_device_status() reports.
+ */
+#ifndef LINATTN_H
+#define LINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define LA_OK 0
+#define LA_ERR_ARG 1         /* null / misaligned pointer, bad stride, inconsistent dims */
+#define LA_ERR_COUNT 2       /* token count 0 or above max_tokens: refused before any launch */
+#define LA_ERR_UNSUPPORTED 3 /* dims outside the compiled instances (cf. the pages' Ok(false)) */
+#define LA_ERR_CUDA 4        /* the CUDA runtime reported an error at launch */
+
+/* ---- activation dtypes ---- */
+#define LA_F32 0
+#define LA_BF16 1
+
+/* ---- device status flags (la_device_status) ---- */
+#define LA_DEV_BAD_SEQLENS 1 /* cu_seqlens not monotone, out of range, or a length > max_seqlen */
+
+/* ABI version of this header (bumped on any signature change). */
+#define LA_ABI_VERSION 1
+int la_abi_version(void);
+
+/* Thread-local description of the last error returned on this host thread ("" if none). */
+const char *la_last_error(void);
+
+/* Synchronises `stream`, then returns and clears the device status flags (LA_DEV_*) raised by
+ * kernels of this library on the current device since the last call. Returns a negative value
+ * if the synchronisation itself failed. Debug/test use: it blocks the host. */
+int la_device_status(uint64_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Causal depthwise conv1d + SiLU over one stream, advancing its conv state.
+ * "glm5next_kda/prefill.rs", conv_prefill launch (conv + SiLU only, bias slot NULL);
+ * "split_prefill.rs", prefill_phase1_conv1d_one.
+ *
+ *   xh = [conv_state (kernel-1 rows, oldest first) ; x (t rows)]
+ *   out[tau][c] = SiLU(bias[c] + sum_{j<kernel} w[c][j] * xh[tau + j][c])   (tap kernel-1 = current)
+ *   conv_state <- xh[t .. t+kernel-2]
+ *
+ * conv_state [kernel-1][channels] (dtype, contiguous, in/out; may be NULL when kernel == 1)
+ * x          [t][x_stride]      (dtype; the first `channels` entries of each row are read)
+ * w          [channels][kernel] (dtype, contiguous)
+ * bias       [channels] (dtype) or NULL for none
+ * out        [t][out_stride]    (dtype; may not alias x)
+ * kernel in 1..4.  Errors: LA_ERR_COUNT (t), LA_ERR_ARG, LA_ERR_UNSUPPORTED (kernel).
+ * ------------------------------------------------------------------------------------------- */
+int la_conv1d_silu_prefill(void *conv_state, const void *x, const void *w, const void *bias,
+                           void *out, int t, int max_tokens, int channels, int kernel,
+                           int64_t x_stride, int64_t out_stride, int dtype, uint64_t stream);
+
+/* Same over B packed streams (cu_seqlens), each with its own conv state: conv_state_ptrs is a
+ * DEVICE array of B device pointers, each to a [kernel-1][channels] state of dtype. */
+int la_conv1d_silu_prefill_varlen(const uint64_t *conv_state_ptrs, const void *x, const void *w,
+                                  const void *bias, void *out, const int32_t *cu_seqlens, int B,
+                                  int total_tokens, int max_tokens, int channels, int kernel,
+                                  int64_t x_stride, int64_t out_stride, int dtype,
+                                  uint64_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Per-(token, head) L2 norm, in place, over the first n_heads*head_dim channels of each row.
+ * "glm5next_kda/prefill.rs", l2 launch (grid q|k heads x tokens, eps = cfg.l2_eps);
+ * "split_prefill.rs", prefill_phase1_l2_batched (over all stacked tokens).
+ *   x[tau][h*head_dim + c] <- x / sqrt(sum_c x^2 + eps)
+ * x [t][row_stride] (dtype). head_dim in {64, 128}. t >= 1.
+ * ------------------------------------------------------------------------------------------- */
+int la_l2norm_heads(void *x, int t, int n_heads, int head_dim, int64_t row_stride, float eps,
+                    int dtype, uint64_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Recurrence arguments shared by the three prefill calls below.
+ *
+ * h_state_ptrs  DEVICE array of B device pointers; pointer s -> fp32 state of stream s laid out
+ *               [Hv][dk][dv] (H = S^T, H[c][d] = S[d][c]); read and updated in place.
+ *               ("split_prefill.rs", prefill_gdn_full_batched: one h-state pointer per stream.)
+ * q, k          [tokens][q_stride], [tokens][k_stride] (dtype): head h at columns h*dk..h*dk+dk-1,
+ *               h < Hk. They may point into one packed [q | k | v] buffer (the split of the
+ *               pages' split_widen becomes pointer arithmetic).
+ * v             [tokens][v_stride] (dtype): v-head j at columns j*dv..j*dv+dv-1, j < Hv.
+ * beta          [tokens][Hv] fp32.
+ * out           [tokens][Hv][dv] (dtype, contiguous). Rows of padding are never written.
+ * GQA           v-head j reads q/k head floor(j*Hk/Hv); Hv must be a multiple of Hk.
+ * scale         output scale (the pages pass 1/sqrt(head_dim) to chunk_scan).
+ * dk, dv        in {64, 128}.
+ * workspace     device scratch of at least la_prefill_workspace_bytes(...) bytes (16-byte
+ *               aligned); may be NULL when that size is 0.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Bytes of device workspace the prefill calls need for these sizes (0 if none). */
+size_t la_prefill_workspace_bytes(int B, int total_tokens, int Hk, int Hv, int dk, int dv,
+                                  int dtype);
+
+/* GDN, B streams of equal length T back to back (tokens s*T .. s*T+T-1 belong to stream s).
+ * "split_prefill.rs", prefill_gdn_full_batched (h_state_ptrs, batch_size, chunk_len).
+ * g [B*T][Hv] fp32 log-decay (alpha = exp(g)). Count rule: 1 <= B*T <= max_tokens. */
+int la_gdn_prefill_batched(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta, void *out, int B,
+                           int T, int max_tokens, int Hk, int Hv, int dk, int dv,
+                           int64_t q_stride, int64_t k_stride, int64_t v_stride, float scale,
+                           int dtype, void *workspace, size_t workspace_bytes, uint64_t stream);
+
+/* GDN over B streams of different lengths driven by cu_seqlens (device) and max_seqlen.
+ * "split_prefill.rs", prefill_gdn_full_batched_fla_varlen (cu_seqlens, total_nt, max_seqlen).
+ * g [total_tokens][Hv] fp32. Count rule: 1 <= total_tokens <= max_tokens. */
+int la_gdn_prefill_varlen(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                          const void *v, const float *g, const float *beta, void *out,
+                          const int32_t *cu_seqlens, int B, int total_tokens, int max_seqlen,
+                          int max_tokens, int Hk, int Hv, int dk, int dv, int64_t q_stride,
+                          int64_t k_stride, int64_t v_stride, float scale, int dtype,
+                          void *workspace, size_t workspace_bytes, uint64_t stream);
+
+/* KDA (per-channel gate) over one stream (cu_seqlens == NULL: tokens 0..total_tokens-1, B = 1)
+ * or B varlen streams. "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill.
+ * gate [total_tokens][Hv][dk] fp32 log-decay per k-channel.
+ * pad_fill: the value the kernels place in q/k/v tile rows at or past a stream's end before
+ *   masking them (the pages fill the padded q/k/v tails with it). Outputs and states do not
+ *   depend on it: positions past the end are ignored in-kernel, by select, never by a zero
+ *   multiply, so NaN works too.
+ * Count rule: 1 <= total_tokens <= max_tokens. */
+int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, const void *v,
+                   const float *gate, const float *beta, void *out, const int32_t *cu_seqlens,
+                   int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,
+                   int dk, int dv, int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                   float scale, float pad_fill, int dtype, void *workspace,
+                   size_t workspace_bytes, uint64_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H */

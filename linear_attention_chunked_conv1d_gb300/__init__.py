@@ -1,0 +1,215 @@
+"""GB300-native chunked gated-delta-rule prefill (GDN / KDA) with a causal conv1d front end.
+
+Thin Python binding of the C ABI in ``include/linattn.h`` (``liblinattn.so``): every function
+here only marshals torch CUDA tensors into raw device pointers, sizes and the current CUDA
+stream, then calls the C entry point of the same name. All arithmetic runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback, and importing fails loudly when the library
+has not been built (``python -m linear_attention_chunked_conv1d_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "LinAttnError", "LA_F32", "LA_BF16", "abi_version", "last_error", "device_status",
+    "conv1d_silu_prefill", "conv1d_silu_prefill_varlen", "l2norm_heads",
+    "prefill_workspace_bytes", "gdn_prefill_batched", "gdn_prefill_varlen", "kda_prefill",
+    "pointer_array", "library_path",
+]
+
+LA_OK, LA_ERR_ARG, LA_ERR_COUNT, LA_ERR_UNSUPPORTED, LA_ERR_CUDA = 0, 1, 2, 3, 4
+LA_F32, LA_BF16 = 0, 1
+LA_DEV_BAD_SEQLENS = 1
+_CODES = {LA_ERR_ARG: "LA_ERR_ARG", LA_ERR_COUNT: "LA_ERR_COUNT",
+          LA_ERR_UNSUPPORTED: "LA_ERR_UNSUPPORTED", LA_ERR_CUDA: "LA_ERR_CUDA"}
+
+
+class LinAttnError(RuntimeError):
+    """A linattn call returned a non-zero status; ``code`` holds it."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_CODES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_u64, _i64, _i32, _f32, _vp, _sz = (ctypes.c_uint64, ctypes.c_int64, ctypes.c_int,
+                                    ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t)
+
+_SIGS = {
+    "la_abi_version": ([], ctypes.c_int),
+    "la_last_error": ([], ctypes.c_char_p),
+    "la_device_status": ([_u64], ctypes.c_int),
+    "la_conv1d_silu_prefill": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i64, _i64,
+                                _i32, _u64], ctypes.c_int),
+    "la_conv1d_silu_prefill_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                       _i32, _i64, _i64, _i32, _u64], ctypes.c_int),
+    "la_l2norm_heads": ([_vp, _i32, _i32, _i32, _i64, _f32, _i32, _u64], ctypes.c_int),
+    "la_prefill_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32, _i32], _sz),
+    "la_gdn_prefill_batched": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                _i32, _i32, _i64, _i64, _i64, _f32, _i32, _vp, _sz, _u64],
+                               ctypes.c_int),
+    "la_gdn_prefill_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                               _i32, _i32, _i32, _i32, _i64, _i64, _i64, _f32, _i32, _vp, _sz,
+                               _u64], ctypes.c_int),
+    "la_kda_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                        _i32, _i32, _i32, _i64, _i64, _i64, _f32, _f32, _i32, _vp, _sz, _u64],
+                       ctypes.c_int),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"linattn CUDA library not built ({LIB_PATH} missing); run "
+                "`python -m linear_attention_chunked_conv1d_gb300.build` — there is no fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != LA_OK:
+        raise LinAttnError(rc, last_error())
+
+
+def abi_version() -> int:
+    return _load().la_abi_version()
+
+
+def last_error() -> str:
+    return _load().la_last_error().decode()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (then clear) the device status flags (LA_DEV_*)."""
+    return _load().la_device_status(_stream(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LA_F32
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    raise TypeError(f"activation dtype {t.dtype}: expected float32 or bfloat16")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _row_stride(t: torch.Tensor) -> int:
+    return t.stride(0)
+
+
+def pointer_array(tensors, device=None) -> torch.Tensor:
+    """Device array of the data pointers of `tensors` (h-state / conv-state lists), stored as
+    int64 (the same 64 bits the C ABI reads as uint64_t)."""
+    ptrs = [t.data_ptr() for t in tensors]
+    dev = device if device is not None else tensors[0].device
+    return torch.tensor(ptrs, dtype=torch.int64, device=dev)
+
+
+def conv1d_silu_prefill(conv_state, x, w, out, *, t=None, bias=None, max_tokens=None,
+                        stream=None) -> None:
+    """Causal conv1d + SiLU over one stream, advancing conv_state [K-1][C] in place.
+
+    x, out: [t][stride] (the first C = w.shape[0] channels are used); w [C][K]."""
+    t = x.shape[0] if t is None else t
+    C, K = w.shape
+    _check(_load().la_conv1d_silu_prefill(
+        _ptr(conv_state), _ptr(x), _ptr(w), _ptr(bias), _ptr(out), t,
+        max_tokens if max_tokens is not None else t, C, K, _row_stride(x), _row_stride(out),
+        _dtype_code(x), _stream(stream)))
+
+
+def conv1d_silu_prefill_varlen(conv_state_ptrs, x, w, out, cu_seqlens, *, bias=None,
+                               total_tokens=None, max_tokens=None, stream=None) -> None:
+    """conv1d_silu_prefill over B packed streams; conv_state_ptrs is a device uint64 array."""
+    B = cu_seqlens.shape[0] - 1
+    total = x.shape[0] if total_tokens is None else total_tokens
+    C, K = w.shape
+    _check(_load().la_conv1d_silu_prefill_varlen(
+        _ptr(conv_state_ptrs), _ptr(x), _ptr(w), _ptr(bias), _ptr(out), _ptr(cu_seqlens), B,
+        total, max_tokens if max_tokens is not None else total, C, K, _row_stride(x),
+        _row_stride(out), _dtype_code(x), _stream(stream)))
+
+
+def l2norm_heads(x, n_heads, head_dim, *, eps=1e-6, t=None, stream=None) -> None:
+    """In-place L2 norm of each (token, head) over the first n_heads*head_dim channels."""
+    t = x.shape[0] if t is None else t
+    _check(_load().la_l2norm_heads(_ptr(x), t, n_heads, head_dim, _row_stride(x), float(eps),
+                                   _dtype_code(x), _stream(stream)))
+
+
+def prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (LA_BF16 if dtype == torch.bfloat16 else LA_F32)
+    return int(_load().la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, code))
+
+
+def gdn_prefill_batched(h_state_ptrs, q, k, v, g, beta, out, *, B, T, Hk, Hv, dk, dv,
+                        scale=None, max_tokens=None, workspace=None, stream=None) -> None:
+    """GDN over B equal-length streams of T tokens; states updated through h_state_ptrs."""
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_load().la_gdn_prefill_batched(
+        _ptr(h_state_ptrs), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out), B, T,
+        max_tokens if max_tokens is not None else B * T, Hk, Hv, dk, dv, _row_stride(q),
+        _row_stride(k), _row_stride(v), float(scale), _dtype_code(q), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def gdn_prefill_varlen(h_state_ptrs, q, k, v, g, beta, out, cu_seqlens, *, max_seqlen, Hk, Hv,
+                       dk, dv, total_tokens=None, scale=None, max_tokens=None, workspace=None,
+                       stream=None) -> None:
+    """GDN over B packed streams of different lengths (cu_seqlens, device int32 [B+1])."""
+    B = cu_seqlens.shape[0] - 1
+    total = q.shape[0] if total_tokens is None else total_tokens
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_load().la_gdn_prefill_varlen(
+        _ptr(h_state_ptrs), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+        _ptr(cu_seqlens), B, total, max_seqlen,
+        max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(q),
+        _row_stride(k), _row_stride(v), float(scale), _dtype_code(q), _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def kda_prefill(h_state_ptrs, q, k, v, gate, beta, out, cu_seqlens=None, *, Hk, Hv, dk, dv,
+                max_seqlen=None, total_tokens=None, scale=None, pad_fill=0.0, max_tokens=None,
+                workspace=None, stream=None) -> None:
+    """KDA (per-channel gate [tok][Hv][dk]) over one stream (cu_seqlens None) or B streams."""
+    B = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    total = q.shape[0] if total_tokens is None else total_tokens
+    max_seqlen = total if max_seqlen is None else max_seqlen
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_load().la_kda_prefill(
+        _ptr(h_state_ptrs), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta), _ptr(out),
+        _ptr(cu_seqlens), B, total, max_seqlen,
+        max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(q),
+        _row_stride(k), _row_stride(v), float(scale), float(pad_fill), _dtype_code(q),
+        _ptr(workspace), ws_bytes, _stream(stream)))

@@ -1,0 +1,294 @@
+// C ABI of linattn: host-side validation (every check before any launch) and dispatch.
+//
+// Error convention follows the pages: "glm5next_kda/prefill.rs" refuses a token count of 0 or
+// above the workspace's max_tokens before any launch (module invariant and the bail! at the top
+// of prefill_with_pad_fill); "split_prefill.rs" returns an error from calls a layer cannot run
+// (prefill_gdn_full_batched's default) — here LA_ERR_UNSUPPORTED for dims outside the compiled
+// instances.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return LA_OK;
+}
+
+// Per-device status word raised by kernels (LA_DEV_*), read and cleared by la_device_status.
+__device__ int g_dev_status;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices];
+std::once_flag g_status_once[kMaxDevices];
+
+int *status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::call_once(g_status_once[dev], [dev] {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dev_status) == cudaSuccess) g_status_ptr[dev] = (int *)p;
+    });
+    return g_status_ptr[dev];
+}
+
+cudaStream_t as_stream(uint64_t s) { return reinterpret_cast<cudaStream_t>(static_cast<uintptr_t>(s)); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int vec_elems(int dtype) { return dtype == LA_BF16 ? 8 : 4; }
+
+int check_dtype(int dtype) {
+    if (dtype != LA_F32 && dtype != LA_BF16)
+        return fail(LA_ERR_ARG, "dtype %d is neither LA_F32 (0) nor LA_BF16 (1)", dtype);
+    return LA_OK;
+}
+
+int check_act_ptr(const void *p, const char *name, bool nullable = false) {
+    if (!p) return nullable ? LA_OK : fail(LA_ERR_ARG, "%s is NULL", name);
+    if (!aligned16(p)) return fail(LA_ERR_ARG, "%s is not 16-byte aligned", name);
+    return LA_OK;
+}
+
+int check_stride(int64_t stride, int64_t width, int dtype, const char *name) {
+    if (stride < width)
+        return fail(LA_ERR_ARG, "%s (%lld) is smaller than the row width (%lld)", name,
+                    (long long)stride, (long long)width);
+    if (stride % vec_elems(dtype))
+        return fail(LA_ERR_ARG, "%s (%lld) is not a multiple of 16 bytes", name, (long long)stride);
+    return LA_OK;
+}
+
+int launch_result(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(LA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+#define LA_TRY(expr)              \
+    do {                          \
+        int _rc = (expr);         \
+        if (_rc != LA_OK) return _rc; \
+    } while (0)
+
+int conv_common(const void *x, const void *w, const void *bias, const void *out, int channels,
+                int kernel, int64_t x_stride, int64_t out_stride, int dtype) {
+    LA_TRY(check_dtype(dtype));
+    if (kernel < 1 || kernel > 4)
+        return fail(LA_ERR_UNSUPPORTED, "conv kernel %d outside the compiled 1..4", kernel);
+    if (channels <= 0) return fail(LA_ERR_ARG, "channels must be positive (got %d)", channels);
+    if (channels % vec_elems(dtype))
+        return fail(LA_ERR_ARG, "channels (%d) is not a multiple of 16 bytes", channels);
+    LA_TRY(check_act_ptr(x, "x"));
+    LA_TRY(check_act_ptr(out, "out"));
+    LA_TRY(check_act_ptr(bias, "bias", true));
+    if (!w) return fail(LA_ERR_ARG, "w is NULL");
+    LA_TRY(check_stride(x_stride, channels, dtype, "x_stride"));
+    LA_TRY(check_stride(out_stride, channels, dtype, "out_stride"));
+    if (x == out) return fail(LA_ERR_ARG, "out may not alias x");
+    return LA_OK;
+}
+
+// Shared checks of the three recurrence calls.
+int rec_common(const uint64_t *h_state_ptrs, const void *q, const void *k, const void *v,
+               const float *g, const float *beta, const void *out, int B, int Hk, int Hv,
+               int dk, int dv, int64_t qs, int64_t ks, int64_t vs, int dtype,
+               const void *workspace, size_t workspace_bytes, size_t need) {
+    LA_TRY(check_dtype(dtype));
+    if (B < 1) return fail(LA_ERR_ARG, "B must be >= 1 (got %d)", B);
+    if (Hk < 1 || Hv < 1) return fail(LA_ERR_ARG, "Hk and Hv must be >= 1 (got %d, %d)", Hk, Hv);
+    if (Hv % Hk) return fail(LA_ERR_ARG, "Hv (%d) is not a multiple of Hk (%d)", Hv, Hk);
+    if ((dk != 64 && dk != 128) || dv != dk)
+        return fail(LA_ERR_UNSUPPORTED, "head dims dk=%d dv=%d: compiled for dk = dv in {64, 128}",
+                    dk, dv);
+    if (!h_state_ptrs) return fail(LA_ERR_ARG, "h_state_ptrs is NULL");
+    LA_TRY(check_act_ptr(q, "q"));
+    LA_TRY(check_act_ptr(k, "k"));
+    LA_TRY(check_act_ptr(v, "v"));
+    LA_TRY(check_act_ptr(out, "out"));
+    if (!g) return fail(LA_ERR_ARG, "g is NULL");
+    if (!beta) return fail(LA_ERR_ARG, "beta is NULL");
+    LA_TRY(check_stride(qs, (int64_t)Hk * dk, dtype, "q_stride"));
+    LA_TRY(check_stride(ks, (int64_t)Hk * dk, dtype, "k_stride"));
+    LA_TRY(check_stride(vs, (int64_t)Hv * dv, dtype, "v_stride"));
+    if (workspace_bytes < need)
+        return fail(LA_ERR_ARG, "workspace of %zu bytes is below the %zu required", workspace_bytes,
+                    need);
+    if (need && (!workspace || !aligned16(workspace)))
+        return fail(LA_ERR_ARG, "workspace is NULL or not 16-byte aligned");
+    return LA_OK;
+}
+
+int run_recurrence(la::RecArgs &a, cudaStream_t st) {
+    a.status = status_ptr();
+    return launch_result(la::launch_chunk_simt(a, st), "chunked recurrence launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int la_abi_version(void) { return LA_ABI_VERSION; }
+
+const char *la_last_error(void) { return g_err; }
+
+int la_device_status(uint64_t stream) {
+    int *p = status_ptr();
+    if (!p) return -1;
+    int h = 0;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemcpyAsync(&h, p, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return -1;
+    if (cudaMemsetAsync(p, 0, sizeof(int), st) != cudaSuccess) return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    return h;
+}
+
+int la_conv1d_silu_prefill(void *conv_state, const void *x, const void *w, const void *bias,
+                           void *out, int t, int max_tokens, int channels, int kernel,
+                           int64_t x_stride, int64_t out_stride, int dtype, uint64_t stream) {
+    if (t <= 0 || t > max_tokens)
+        return fail(LA_ERR_COUNT, "conv1d of %d tokens does not fit max_tokens %d", t, max_tokens);
+    LA_TRY(conv_common(x, w, bias, out, channels, kernel, x_stride, out_stride, dtype));
+    if (kernel > 1) LA_TRY(check_act_ptr(conv_state, "conv_state"));
+    la::ConvArgs a{};
+    a.single_state = conv_state;
+    a.x = x; a.w = w; a.bias = bias; a.out = out;
+    a.cu = nullptr; a.B = 1; a.total = t; a.channels = channels; a.kernel = kernel;
+    a.x_stride = x_stride; a.out_stride = out_stride; a.dtype = dtype;
+    a.status = status_ptr();
+    return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu launch");
+}
+
+int la_conv1d_silu_prefill_varlen(const uint64_t *conv_state_ptrs, const void *x, const void *w,
+                                  const void *bias, void *out, const int32_t *cu_seqlens, int B,
+                                  int total_tokens, int max_tokens, int channels, int kernel,
+                                  int64_t x_stride, int64_t out_stride, int dtype,
+                                  uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "conv1d of %d tokens does not fit max_tokens %d", total_tokens,
+                    max_tokens);
+    LA_TRY(conv_common(x, w, bias, out, channels, kernel, x_stride, out_stride, dtype));
+    if (B < 1) return fail(LA_ERR_ARG, "B must be >= 1 (got %d)", B);
+    if (!cu_seqlens) return fail(LA_ERR_ARG, "cu_seqlens is NULL");
+    if (kernel > 1 && !conv_state_ptrs) return fail(LA_ERR_ARG, "conv_state_ptrs is NULL");
+    la::ConvArgs a{};
+    a.state_ptrs = conv_state_ptrs;
+    a.x = x; a.w = w; a.bias = bias; a.out = out;
+    a.cu = cu_seqlens; a.B = B; a.total = total_tokens; a.channels = channels; a.kernel = kernel;
+    a.x_stride = x_stride; a.out_stride = out_stride; a.dtype = dtype;
+    a.status = status_ptr();
+    return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu launch");
+}
+
+int la_l2norm_heads(void *x, int t, int n_heads, int head_dim, int64_t row_stride, float eps,
+                    int dtype, uint64_t stream) {
+    if (t <= 0) return fail(LA_ERR_COUNT, "l2norm of %d tokens", t);
+    LA_TRY(check_dtype(dtype));
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_UNSUPPORTED, "head_dim %d: compiled for 64 and 128", head_dim);
+    if (n_heads < 1) return fail(LA_ERR_ARG, "n_heads must be >= 1 (got %d)", n_heads);
+    LA_TRY(check_act_ptr(x, "x"));
+    LA_TRY(check_stride(row_stride, (int64_t)n_heads * head_dim, dtype, "row_stride"));
+    if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
+    la::L2Args a{x, t, n_heads, head_dim, row_stride, eps, dtype};
+    return launch_result(la::launch_l2norm_heads(a, as_stream(stream)), "l2norm launch");
+}
+
+size_t la_prefill_workspace_bytes(int B, int total_tokens, int Hk, int Hv, int dk, int dv,
+                                  int dtype) {
+    (void)B; (void)total_tokens; (void)Hk; (void)Hv; (void)dk; (void)dv; (void)dtype;
+    return 0;
+}
+
+int la_gdn_prefill_batched(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta, void *out, int B,
+                           int T, int max_tokens, int Hk, int Hv, int dk, int dv,
+                           int64_t q_stride, int64_t k_stride, int64_t v_stride, float scale,
+                           int dtype, void *workspace, size_t workspace_bytes, uint64_t stream) {
+    if (B < 1 || T < 1 || (int64_t)B * T > max_tokens)
+        return fail(LA_ERR_COUNT, "batched prefill of %d x %d tokens does not fit max_tokens %d",
+                    B, T, max_tokens);
+    const int total = B * T;
+    size_t need = la_prefill_workspace_bytes(B, total, Hk, Hv, dk, dv, dtype);
+    LA_TRY(rec_common(h_state_ptrs, q, k, v, g, beta, out, B, Hk, Hv, dk, dv, q_stride, k_stride,
+                      v_stride, dtype, workspace, workspace_bytes, need));
+    la::RecArgs a{};
+    a.h_ptrs = h_state_ptrs; a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
+    a.cu = nullptr; a.B = B; a.T_each = T; a.total = total; a.max_seqlen = T;
+    a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.q_stride = q_stride; a.k_stride = k_stride; a.v_stride = v_stride;
+    a.scale = scale; a.pad_fill = 0.f; a.dtype = dtype; a.kda = false;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    return run_recurrence(a, as_stream(stream));
+}
+
+int la_gdn_prefill_varlen(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                          const void *v, const float *g, const float *beta, void *out,
+                          const int32_t *cu_seqlens, int B, int total_tokens, int max_seqlen,
+                          int max_tokens, int Hk, int Hv, int dk, int dv, int64_t q_stride,
+                          int64_t k_stride, int64_t v_stride, float scale, int dtype,
+                          void *workspace, size_t workspace_bytes, uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "varlen prefill of %d tokens does not fit max_tokens %d",
+                    total_tokens, max_tokens);
+    if (!cu_seqlens) return fail(LA_ERR_ARG, "cu_seqlens is NULL");
+    if (max_seqlen < 1 || max_seqlen > total_tokens)
+        return fail(LA_ERR_ARG, "max_seqlen %d outside 1..total_tokens (%d)", max_seqlen,
+                    total_tokens);
+    size_t need = la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype);
+    LA_TRY(rec_common(h_state_ptrs, q, k, v, g, beta, out, B, Hk, Hv, dk, dv, q_stride, k_stride,
+                      v_stride, dtype, workspace, workspace_bytes, need));
+    la::RecArgs a{};
+    a.h_ptrs = h_state_ptrs; a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
+    a.cu = cu_seqlens; a.B = B; a.T_each = 0; a.total = total_tokens; a.max_seqlen = max_seqlen;
+    a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.q_stride = q_stride; a.k_stride = k_stride; a.v_stride = v_stride;
+    a.scale = scale; a.pad_fill = 0.f; a.dtype = dtype; a.kda = false;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    return run_recurrence(a, as_stream(stream));
+}
+
+int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, const void *v,
+                   const float *gate, const float *beta, void *out, const int32_t *cu_seqlens,
+                   int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,
+                   int dk, int dv, int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                   float scale, float pad_fill, int dtype, void *workspace,
+                   size_t workspace_bytes, uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "prefill of %d tokens does not fit a workspace built for %d",
+                    total_tokens, max_tokens);
+    if (!cu_seqlens) {
+        if (B != 1) return fail(LA_ERR_ARG, "cu_seqlens NULL requires B == 1 (got %d)", B);
+        max_seqlen = total_tokens;
+    } else if (max_seqlen < 1 || max_seqlen > total_tokens) {
+        return fail(LA_ERR_ARG, "max_seqlen %d outside 1..total_tokens (%d)", max_seqlen,
+                    total_tokens);
+    }
+    size_t need = la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype);
+    LA_TRY(rec_common(h_state_ptrs, q, k, v, gate, beta, out, B, Hk, Hv, dk, dv, q_stride,
+                      k_stride, v_stride, dtype, workspace, workspace_bytes, need));
+    la::RecArgs a{};
+    a.h_ptrs = h_state_ptrs; a.q = q; a.k = k; a.v = v; a.g = gate; a.beta = beta; a.out = out;
+    a.cu = cu_seqlens; a.B = B; a.T_each = cu_seqlens ? 0 : total_tokens; a.total = total_tokens;
+    a.max_seqlen = max_seqlen;
+    a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.q_stride = q_stride; a.k_stride = k_stride; a.v_stride = v_stride;
+    a.scale = scale; a.pad_fill = pad_fill; a.dtype = dtype; a.kda = true;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    return run_recurrence(a, as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,78 @@
+// Shared device helpers of the linattn library (not part of the C ABI).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/linattn.h"
+
+namespace la {
+
+// 16-byte vector of activations, widened to fp32.
+template <typename T> struct Vec16;
+
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void load(const float *p, float *f) {
+        float4 v = *reinterpret_cast<const float4 *>(p);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+    __device__ __forceinline__ static void store(float *p, const float *f) {
+        *reinterpret_cast<float4 *>(p) = make_float4(f[0], f[1], f[2], f[3]);
+    }
+};
+
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *f) {
+        uint4 v = *reinterpret_cast<const uint4 *>(p);
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 t = __bfloat1622float2(h[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16 *p, const float *f) {
+        uint4 v;
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        *reinterpret_cast<uint4 *>(p) = v;
+    }
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Raises a device status flag (LA_DEV_*). `status` points at the library's per-device word.
+__device__ __forceinline__ void raise_status(int *status, int flag) {
+    if (status) atomicOr(status, flag);
+}
+
+// Token range of stream s: explicit cu_seqlens (varlen) or s*T_each (batched / single).
+// Returns false (and raises LA_DEV_BAD_SEQLENS) if the offsets are out of bounds.
+__device__ __forceinline__ bool stream_range(const int32_t *cu, int s, int T_each, int total,
+                                             int max_seqlen, int *status, int &t0, int &len) {
+    if (!cu) {
+        t0 = s * T_each;
+        len = T_each;
+        return true;
+    }
+    int a = cu[s], b = cu[s + 1];
+    if (a < 0 || b < a || b > total || (b - a) > max_seqlen) {
+        raise_status(status, LA_DEV_BAD_SEQLENS);
+        return false;
+    }
+    t0 = a;
+    len = b - a;
+    return true;
+}
+
+}  // namespace la

@@ -1,0 +1,51 @@
+// Internal launcher interface between the C ABI (abi.cu) and the kernels. Not exported.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace la {
+
+struct ConvArgs {
+    const uint64_t *state_ptrs;  // varlen: device array of B state pointers; else nullptr
+    void *single_state;          // single stream: the state
+    const void *x, *w, *bias;
+    void *out;
+    const int32_t *cu;  // nullptr: one stream of `total` tokens
+    int B, total, channels, kernel;
+    int64_t x_stride, out_stride;
+    int dtype;
+    int *status;
+};
+cudaError_t launch_conv1d_silu(const ConvArgs &a, cudaStream_t st);
+
+struct L2Args {
+    void *x;
+    int t, n_heads, head_dim;
+    int64_t row_stride;
+    float eps;
+    int dtype;
+};
+cudaError_t launch_l2norm_heads(const L2Args &a, cudaStream_t st);
+
+struct RecArgs {
+    const uint64_t *h_ptrs;
+    const void *q, *k, *v;
+    const float *g;  // GDN [tok][Hv]; KDA [tok][Hv][dk]
+    const float *beta;
+    void *out;
+    const int32_t *cu;  // nullptr: batched, stream s = tokens s*T_each ..
+    int B, T_each, total, max_seqlen;
+    int Hk, Hv, dk, dv;
+    int64_t q_stride, k_stride, v_stride;
+    float scale, pad_fill;
+    int dtype;
+    bool kda;
+    void *workspace;
+    size_t workspace_bytes;
+    int *status;
+};
+// CUDA-core chunked kernel (fp32 and bf16 activations).
+cudaError_t launch_chunk_simt(const RecArgs &a, cudaStream_t st);
+
+}  // namespace la

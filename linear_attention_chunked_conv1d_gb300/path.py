@@ -1,0 +1,83 @@
+"""One prefill pass of a GDN/KDA layer's hot path through the C ABI.
+
+Order of the steps as on "glm5next_kda/prefill.rs" (Glm5NextKdaLayer::prefill_with_pad_fill)
+and "split_prefill.rs" (prefill_phase1_conv1d_one per request, prefill_phase1_l2_batched, then
+prefill_gdn_full_batched when all streams have one length, else the varlen call):
+
+    conv1d + SiLU (per stream, carried conv state)  ->  L2 over the q|k heads  ->  recurrence
+
+The packed front-end output [tokens][q heads | k heads | v heads] is handed to the recurrence
+as three strided views (q, k, v), which is all the pages' split_widen step amounts to here.
+This module only sequences the library calls; it holds no arithmetic.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import (conv1d_silu_prefill, conv1d_silu_prefill_varlen, gdn_prefill_batched,
+               gdn_prefill_varlen, kda_prefill, l2norm_heads, pointer_array,
+               prefill_workspace_bytes)
+
+
+class PrefillPass:
+    """Buffers and state pointers for repeated passes over one packed batch on one device.
+
+    `inputs` holds device tensors: x [T][cd], conv_w [cd][K], conv_state [B][K-1][cd],
+    h [B][Hv][d][d] (fp32), g, beta, cu_seqlens, plus `lengths` (host list)."""
+
+    def __init__(self, wl, inputs: dict, *, eps: float = 1e-6, pad_fill: float = 0.0):
+        self.wl = wl
+        self.inp = inputs
+        self.eps = eps
+        self.pad_fill = pad_fill
+        x = inputs["x"]
+        self.T = x.shape[0]
+        self.lengths = list(inputs["lengths"])
+        self.max_seqlen = max(self.lengths)
+        dev = x.device
+        self.conv_out = torch.empty_like(x)
+        self.out = torch.empty(self.T, wl.Hv, wl.d, dtype=x.dtype, device=dev)
+        B = wl.B
+        self.conv_state_ptrs = pointer_array([inputs["conv_state"][s] for s in range(B)])
+        self.h_ptrs = pointer_array([inputs["h"][s] for s in range(B)])
+        nbytes = prefill_workspace_bytes(B, self.T, wl.Hk, wl.Hv, wl.d, wl.d, x.dtype)
+        self.workspace = (torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes
+                          else None)
+        hk = wl.Hk * wl.d
+        self.q = self.conv_out[:, :hk]
+        self.k = self.conv_out[:, hk:2 * hk]
+        self.v = self.conv_out[:, 2 * hk:]
+        self.scale = 1.0 / math.sqrt(wl.d)
+
+    def front_end(self, stream=None):
+        wl, inp = self.wl, self.inp
+        if wl.B == 1:
+            conv1d_silu_prefill(inp["conv_state"][0], inp["x"], inp["conv_w"], self.conv_out,
+                                stream=stream)
+        else:
+            conv1d_silu_prefill_varlen(self.conv_state_ptrs, inp["x"], inp["conv_w"],
+                                       self.conv_out, inp["cu_seqlens"], stream=stream)
+        l2norm_heads(self.conv_out, 2 * wl.Hk, wl.d, eps=self.eps, stream=stream)
+
+    def recurrence(self, stream=None):
+        wl, inp = self.wl, self.inp
+        d = wl.d
+        common = dict(Hk=wl.Hk, Hv=wl.Hv, dk=d, dv=d, scale=self.scale, workspace=self.workspace,
+                      stream=stream)
+        if wl.variant == "kda":
+            kda_prefill(self.h_ptrs, self.q, self.k, self.v, inp["g"], inp["beta"], self.out,
+                        None if wl.B == 1 else inp["cu_seqlens"], max_seqlen=self.max_seqlen,
+                        pad_fill=self.pad_fill, **common)
+        elif wl.batched:
+            gdn_prefill_batched(self.h_ptrs, self.q, self.k, self.v, inp["g"], inp["beta"],
+                                self.out, B=wl.B, T=self.lengths[0], **common)
+        else:
+            gdn_prefill_varlen(self.h_ptrs, self.q, self.k, self.v, inp["g"], inp["beta"],
+                               self.out, inp["cu_seqlens"], max_seqlen=self.max_seqlen, **common)
+
+    def run(self, stream=None):
+        self.front_end(stream)
+        self.recurrence(stream)
+        return self.out

@@ -1,0 +1,135 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol include/linattn.h
+declares, and refuses bad counts and arguments on the host before any CUDA call.
+
+Refusal rule: "glm5next_kda/prefill.rs" — a call covers 1..=max_tokens tokens and any other
+count is refused before a launch (module invariant; the bail! of prefill_with_pad_fill).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "linattn.h")
+
+A = 0x10000  # a 16-byte-aligned fake address: never dereferenced, calls are refused first
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib(built_lib):
+    import linear_attention_chunked_conv1d_gb300 as la
+    la._load()
+    return la
+
+
+def test_header_declares_the_pages_calls():
+    syms = declared_symbols()
+    for name in ["la_conv1d_silu_prefill", "la_conv1d_silu_prefill_varlen", "la_l2norm_heads",
+                 "la_gdn_prefill_batched", "la_gdn_prefill_varlen", "la_kda_prefill"]:
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(built_lib):
+    cdll = ctypes.CDLL(built_lib)
+    for name in declared_symbols():
+        assert hasattr(cdll, name), name
+    nm = subprocess.run(["nm", "-D", "--defined-only", built_lib], capture_output=True,
+                        text=True).stdout
+    for name in declared_symbols():
+        assert re.search(rf"\bT {name}$", nm, flags=re.M), name
+
+
+def test_abi_version(lib):
+    assert lib.abi_version() == 1
+
+
+def _rc_conv(lib, t, max_tokens, **kw):
+    args = dict(conv_state=A, x=A, w=A, bias=None, out=A * 2, channels=64, kernel=4,
+                x_stride=64, out_stride=64, dtype=1)
+    args.update(kw)
+    return lib._load().la_conv1d_silu_prefill(
+        args["conv_state"], args["x"], args["w"], args["bias"], args["out"], t, max_tokens,
+        args["channels"], args["kernel"], args["x_stride"], args["out_stride"], args["dtype"], 0)
+
+
+def test_conv_refuses_counts(lib):
+    assert _rc_conv(lib, 0, 10) == lib.LA_ERR_COUNT
+    assert _rc_conv(lib, 11, 10) == lib.LA_ERR_COUNT
+    assert _rc_conv(lib, -3, 10) == lib.LA_ERR_COUNT
+    assert "max_tokens" in lib.last_error()
+
+
+def test_conv_refuses_bad_args(lib):
+    assert _rc_conv(lib, 5, 10, x=A + 2) == lib.LA_ERR_ARG           # misaligned
+    assert _rc_conv(lib, 5, 10, x=None) == lib.LA_ERR_ARG            # null
+    assert _rc_conv(lib, 5, 10, channels=60) == lib.LA_ERR_ARG       # not 16 B of bf16
+    assert _rc_conv(lib, 5, 10, x_stride=32) == lib.LA_ERR_ARG       # stride < width
+    assert _rc_conv(lib, 5, 10, out=A) == lib.LA_ERR_ARG             # aliasing
+    assert _rc_conv(lib, 5, 10, dtype=7) == lib.LA_ERR_ARG
+    assert _rc_conv(lib, 5, 10, kernel=5) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_conv(lib, 5, 10, conv_state=None) == lib.LA_ERR_ARG
+
+
+def test_l2_refusals(lib):
+    f = lib._load().la_l2norm_heads
+    assert f(A, 0, 2, 128, 256, 1e-6, 1, 0) == lib.LA_ERR_COUNT
+    assert f(A, 4, 2, 96, 256, 1e-6, 1, 0) == lib.LA_ERR_UNSUPPORTED
+    assert f(A, 4, 2, 128, 200, 1e-6, 1, 0) == lib.LA_ERR_ARG
+    assert f(A + 8, 4, 2, 128, 256, 1e-6, 1, 0) == lib.LA_ERR_ARG
+
+
+def _rc_gdn_batched(lib, B, T, max_tokens, **kw):
+    a = dict(Hk=2, Hv=4, dk=128, dv=128, qs=1024, ks=1024, vs=512, dtype=1, ws=None, wsb=0)
+    a.update(kw)
+    return lib._load().la_gdn_prefill_batched(A, A, A, A, A, A, A * 2, B, T, max_tokens, a["Hk"],
+                                              a["Hv"], a["dk"], a["dv"], a["qs"], a["ks"],
+                                              a["vs"], 0.1, a["dtype"], a["ws"], a["wsb"], 0)
+
+
+def test_gdn_batched_refusals(lib):
+    assert _rc_gdn_batched(lib, 2, 0, 100) == lib.LA_ERR_COUNT
+    assert _rc_gdn_batched(lib, 0, 5, 100) == lib.LA_ERR_COUNT
+    assert _rc_gdn_batched(lib, 4, 30, 100) == lib.LA_ERR_COUNT     # 120 > 100
+    assert _rc_gdn_batched(lib, 2, 8, 100, Hv=3) == lib.LA_ERR_ARG   # Hv % Hk
+    assert _rc_gdn_batched(lib, 2, 8, 100, dk=96, dv=96) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_gdn_batched(lib, 2, 8, 100, dk=128, dv=64) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_gdn_batched(lib, 2, 8, 100, qs=100) == lib.LA_ERR_ARG
+
+
+def test_varlen_and_kda_refusals(lib):
+    L = lib._load()
+    # total 0 / above max_tokens
+    assert L.la_gdn_prefill_varlen(A, A, A, A, A, A, A * 2, A, 3, 0, 1, 10, 1, 1, 64, 64, 64, 64,
+                                   64, 1.0, 1, None, 0, 0) == lib.LA_ERR_COUNT
+    assert L.la_gdn_prefill_varlen(A, A, A, A, A, A, A * 2, A, 3, 11, 5, 10, 1, 1, 64, 64, 64, 64,
+                                   64, 1.0, 1, None, 0, 0) == lib.LA_ERR_COUNT
+    # null cu_seqlens
+    assert L.la_gdn_prefill_varlen(A, A, A, A, A, A, A * 2, None, 3, 9, 5, 10, 1, 1, 64, 64, 64,
+                                   64, 64, 1.0, 1, None, 0, 0) == lib.LA_ERR_ARG
+    # max_seqlen beyond total
+    assert L.la_gdn_prefill_varlen(A, A, A, A, A, A, A * 2, A, 3, 9, 10, 10, 1, 1, 64, 64, 64,
+                                   64, 64, 1.0, 1, None, 0, 0) == lib.LA_ERR_ARG
+    # KDA: count refusal, and B != 1 without cu_seqlens
+    assert L.la_kda_prefill(A, A, A, A, A, A, A * 2, None, 1, 0, 1, 10, 1, 1, 64, 64, 64, 64, 64,
+                            1.0, 0.0, 1, None, 0, 0) == lib.LA_ERR_COUNT
+    assert L.la_kda_prefill(A, A, A, A, A, A, A * 2, None, 2, 5, 5, 10, 1, 1, 64, 64, 64, 64, 64,
+                            1.0, 0.0, 1, None, 0, 0) == lib.LA_ERR_ARG
+    assert "max_tokens" in lib.last_error() or "B == 1" in lib.last_error()
+
+
+def test_binding_raises_typed_error(lib):
+    with pytest.raises(lib.LinAttnError) as ei:
+        lib._check(lib.LA_ERR_COUNT)
+    assert ei.value.code == lib.LA_ERR_COUNT
+
+
+def test_workspace_query(lib):
+    assert lib.prefill_workspace_bytes(4, 1000, 16, 32, 128, 128, lib.LA_BF16) >= 0

@@ -1,0 +1,80 @@
+"""Full-size workloads on the GPU, in the launch configuration the bench times (PrefillPass:
+conv1d+SiLU -> L2 -> recurrence through the C ABI), checked against the oracle on sampled
+(stream, v-head) units: every sampled unit's outputs, final state and the stream's conv state.
+Units are independent, so a sample is checked exactly as the whole would be.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_chunked_conv1d_gb300.inputs import WORKLOADS, make_inputs
+from linear_attention_chunked_conv1d_gb300.path import PrefillPass
+from tests.helpers import TOL, f64, max_abs, oracle_front, oracle_recurrence, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_units(wl, lengths):
+    if wl.B == 1:
+        streams = [0]
+    else:
+        order = np.argsort(lengths)
+        streams = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2])})
+    heads = sorted({0, wl.Hv // 2 + 1, wl.Hv - 1})
+    return streams, heads
+
+
+def check_workload(wl, cuda, pad_fill=0.0, seed=0):
+    inp = make_inputs(wl, device=cuda, seed=seed)
+    lengths = inp["lengths"]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    streams, heads = sample_units(wl, lengths)
+    keep = {s: dict(x=inp["x"][cu[s]:cu[s + 1]].cpu(), conv_state=inp["conv_state"][s].cpu(),
+                    h=inp["h"][s].cpu(), g=inp["g"][cu[s]:cu[s + 1]].cpu(),
+                    beta=inp["beta"][cu[s]:cu[s + 1]].cpu()) for s in streams}
+    conv_w = inp["conv_w"].cpu()
+    p = PrefillPass(wl, inp, pad_fill=pad_fill)
+    p.run()
+    torch.cuda.synchronize()
+    act = wl.dtype
+    d = wl.d
+    worst_o, worst_h = 0.0, 0.0
+    for s in streams:
+        k_ = keep[s]
+        L = lengths[s]
+        q, k, v, new_conv = oracle_front(k_["x"], conv_w, k_["conv_state"][None], [L], wl.Hk,
+                                         wl.Hv, d, 1e-6, act)
+        np.testing.assert_array_equal(f64(inp["conv_state"][s].cpu()), new_conv[0])
+        ref_o, ref_h = oracle_recurrence(k_["h"][None], q, k, v, k_["g"], k_["beta"], [L],
+                                         1.0 / math.sqrt(d), wl.variant == "kda", heads=heads)
+        got_o = f64(p.out[cu[s]:cu[s + 1]][:, heads].cpu())
+        got_h = f64(inp["h"][s][heads].cpu())
+        worst_o = max(worst_o, max_abs(got_o, ref_o))
+        worst_h = max(worst_h, rel_frob(got_h, ref_h[0]))
+    tol = TOL[act]
+    assert worst_o <= tol["out"], f"{wl.name}: max |o - o_ref| = {worst_o:.3g}"
+    assert worst_h <= tol["state"], f"{wl.name}: state rel. Frobenius error {worst_h:.3g}"
+    return p
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workload_full_size_sampled_parity(cuda, name):
+    check_workload(WORKLOADS[name], cuda)
+    torch.cuda.empty_cache()
+
+
+def test_kda_t4096_pad_fill_identical(cuda):
+    """T = 4096 is a multiple of the chunk (no pad tail), so also run T = 4001."""
+    for T in (4096, 4001):
+        wl = WORKLOADS["kda_t4096_h32_d128"].replace(lengths=f"fixed:{T}")
+        outs = []
+        for pf in (0.0, 1e3):
+            inp = make_inputs(wl, device="cuda", seed=1)
+            p = PrefillPass(wl, inp, pad_fill=pf)
+            p.run()
+            torch.cuda.synchronize()
+            outs.append((p.out.clone(), inp["h"].clone(), inp["conv_state"].clone()))
+        for a, b in zip(*outs):
+            assert torch.equal(a, b)
