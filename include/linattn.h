@@ -58,6 +58,8 @@ extern "C" {
 
 /* ---- device status flags (la_device_status) ---- */
 #define LA_DEV_BAD_SEQLENS 1 /* cu_seqlens not monotone, out of range, or a length > max_seqlen */
+#define LA_DEV_TIMEOUT 2     /* a bounded wait inside a kernel gave up; that kernel's results are
+                                incomplete (never expected; reported instead of hanging) */
 
 /* ABI version of this header (bumped on any signature change). */
 #define LA_ABI_VERSION 1

@@ -132,8 +132,16 @@ int rec_common(const uint64_t *h_state_ptrs, const void *q, const void *k, const
     return LA_OK;
 }
 
+bool uses_tensor_cores(int dtype, int dk, int dv) {
+    la::RecArgs a{};
+    a.dtype = dtype; a.dk = dk; a.dv = dv;
+    return la::chunk_tc_supported(a);
+}
+
 int run_recurrence(la::RecArgs &a, cudaStream_t st) {
     a.status = status_ptr();
+    if (la::chunk_tc_supported(a))
+        return launch_result(la::launch_chunk_tc(a, st), "chunked recurrence (tcgen05) launch");
     return launch_result(la::launch_chunk_simt(a, st), "chunked recurrence launch");
 }
 
@@ -209,8 +217,9 @@ int la_l2norm_heads(void *x, int t, int n_heads, int head_dim, int64_t row_strid
 
 size_t la_prefill_workspace_bytes(int B, int total_tokens, int Hk, int Hv, int dk, int dv,
                                   int dtype) {
-    (void)B; (void)total_tokens; (void)Hk; (void)Hv; (void)dk; (void)dv; (void)dtype;
-    return 0;
+    (void)total_tokens; (void)Hk; (void)Hv;
+    if (B < 1) return 0;
+    return uses_tensor_cores(dtype, dk, dv) ? la::chunk_tc_workspace_bytes(B) : 0;
 }
 
 int la_gdn_prefill_batched(const uint64_t *h_state_ptrs, const void *q, const void *k,

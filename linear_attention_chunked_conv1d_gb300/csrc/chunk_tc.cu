@@ -1,0 +1,690 @@
+// Chunked gated delta rule on the 5th-generation tensor cores (tcgen05 + TMEM), bf16
+// activations, head dim 128, GDN (scalar gate) and KDA (per-channel gate).
+//
+// Pages: "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill — chunk_prepare
+// (cumulative gate, WY factors per chunk) then chunk_scan (one block per head walking the
+// chunks, state updated in place); "split_prefill.rs", prefill_gdn_full_batched and
+// prefill_gdn_full_batched_fla_varlen (streams through a device array of h-state pointers,
+// cu_seqlens). Here prepare and scan are fused in one persistent block per SM that claims
+// (stream, v-head) units, longest stream first.
+//
+// Per chunk of C = 64 tokens (t, i: tokens; c: k-channel; d: v-channel; S = H^T [d][c], fp32,
+// resident in TMEM for the whole unit; gc: inclusive cumulative log-gate, pad rows g = 0):
+//   D1 = [K ; Q] K^T                     tensor core (GDN: bf16 inputs as loaded;
+//                                        KDA: tf32, with decays split at the mid row m:
+//                                        [K e^{gc-gc_m} ; Q e^{gc-gc_m}] (K e^{gc_m-gc})^T)
+//   A  = strictly-lower(beta_t e^{gc_t-gc_i} D1_KK),  P = lower(e^{gc_t-gc_i} D1_QK)
+//   T  = (I + A)^{-1}                    CUDA cores, forward substitution per column
+//   D2 = S [K e^gc ; Q e^gc]^T           tensor core (tf32, A operand read from TMEM)
+//   R^T = beta (V^T - D2[:, :64])        CUDA cores -> TMEM
+//   U'^T = R^T T^T                       tensor core
+//   O^T = D2[:, 64:] + U'^T P^T          tensor core, accumulating into D2
+//   S  <- S diag(e^{gc_L}) + U'^T (K e^{gc_L - gc})     tensor core, accumulating into S
+//   o  = scale O                          epilogue
+// which is the token recurrence S_t = S_{t-1} diag(a_t)(I - b_t k_t k_t^T) + b_t v_t k_t^T,
+// o_t = scale S_t q_t, unrolled over the chunk. Every exponent is <= 0 except the KDA
+// mid-row split, whose range is checked per chunk; a chunk whose half-chunk decay exceeds
+// e^80 in some channel takes an exact pairwise-exponent path for D1 on the CUDA cores.
+//
+// Precision: operands that are raw bf16 inputs use kind::f16; operands derived from fp32
+// values (state, T, U', decayed keys) use kind::tf32 with round-to-nearest conversion,
+// accumulation is fp32. Rows at or past a stream's end are removed by selects.
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace la {
+
+namespace {
+
+constexpr int TC_C = 64;         // chunk
+constexpr int TC_D = 128;        // dk = dv
+constexpr int TC_THREADS = 256;  // 8 warps: warp w owns TMEM lanes 32*(w%4).. and column half w/4
+constexpr uint64_t WAIT_NS = 2000000000ull;
+
+// TMEM columns
+constexpr uint32_t COL_S = 0, COL_D2 = 128, COL_RU = 256, COL_D6 = 320, COL_D1 = 384;
+constexpr uint32_t TMEM_COLS = 512;
+
+// shared memory layout (bytes from a 1024-aligned base)
+constexpr uint32_t SM_KQ = 0;                    // bf16 SW128 [128 rows: K | Q][128]
+constexpr uint32_t SM_V = SM_KQ + 32768;         // bf16 SW128 [64][128]
+constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: Kg | Qg][128]; KDA: Kl|Ql
+constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t] (Kdec^T); KDA: Kr
+constexpr uint32_t SM_P = SM_KDT + 32768;        // tf32 SW128 [64 t][64 i]
+constexpr uint32_t SM_T = SM_P + 16384;          // tf32 SW128 [64 t][64 i]
+constexpr uint32_t SM_AT = SM_T + 16384;         // fp32 A^T split by row parity: [64 i][4][20]
+constexpr uint32_t AT_I = 80, AT_P = 20;         // floats per i row / per row class
+constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_I * 4;
+// small region (floats)
+constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 256,
+                   SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704, SF_WARP = 832,
+                   SF_END = 840;
+constexpr uint32_t SM_BYTES = SM_SMALL + SF_END * 4 + 64;  // + mbarriers, flags, tmem base
+constexpr size_t TC_SMEM = SM_BYTES + 1024;                // alignment slack
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct TcParams {
+    RecArgs a;
+    const int32_t *perm;  // streams sorted by decreasing length
+    int *counter;         // unit claim counter (zeroed by the order kernel)
+    int num_units;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Byte offsets of one column (element k) of a K-major SW128 tile with R rows: row t sits at
+// off[t % 8] + (t / 8) * 1024, so fully unrolled walks down a column need no address math.
+struct ColWalk {
+    uint32_t off[8];
+    __device__ __forceinline__ void init(uint32_t base, uint32_t k, uint32_t R, uint32_t es) {
+#pragma unroll
+        for (uint32_t r = 0; r < 8; ++r) off[r] = base + tc::sw128_offset(r, k, R, es);
+    }
+    __device__ __forceinline__ uint32_t at(int t) const {
+        return off[t & 7] + static_cast<uint32_t>(t >> 3) * 1024u;
+    }
+};
+
+__device__ __forceinline__ float ld_bf16(const unsigned char *sm, uint32_t off) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off));
+}
+__device__ __forceinline__ void st_tf32(unsigned char *sm, uint32_t off, float v) {
+    *reinterpret_cast<float *>(sm + off) = tc::to_tf32(v);
+}
+
+// Issue the K, Q (k-head kh) and V (v-head j) rows of one chunk as 16-byte async copies into
+// the swizzled tiles; rows >= n are zero-filled (their source is never read).
+__device__ __forceinline__ void load_kq(const RecArgs &a, unsigned char *sm, int tok0, int n,
+                                        int kh, int tid) {
+    const __nv_bfloat16 *kp = reinterpret_cast<const __nv_bfloat16 *>(a.k) + (int64_t)kh * TC_D;
+    const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) + (int64_t)kh * TC_D;
+    const uint32_t base = tc::smem_u32(sm + SM_KQ);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int idx = tid + TC_THREADS * m;  // 0..2047
+        const int which = idx >> 10, rem = idx & 1023;
+        const int row = rem >> 4, ch = rem & 15;
+        const bool valid = row < n;
+        const int srow = tok0 + (valid ? row : 0);
+        const __nv_bfloat16 *src =
+            (which ? qp : kp) + (int64_t)srow * (which ? a.q_stride : a.k_stride) + ch * 8;
+        cp_async16(base + tc::sw128_offset(which * 64 + row, ch * 8, 128, 2), src, valid);
+    }
+}
+__device__ __forceinline__ void load_v(const RecArgs &a, unsigned char *sm, int tok0, int n,
+                                       int j, int tid) {
+    const __nv_bfloat16 *vp = reinterpret_cast<const __nv_bfloat16 *>(a.v) + (int64_t)j * TC_D;
+    const uint32_t base = tc::smem_u32(sm + SM_V);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int idx = tid + TC_THREADS * m;  // 0..1023
+        const int row = idx >> 4, ch = idx & 15;
+        const bool valid = row < n;
+        const int srow = tok0 + (valid ? row : 0);
+        cp_async16(base + tc::sw128_offset(row, ch * 8, 64, 2),
+                   vp + (int64_t)srow * a.v_stride + ch * 8, valid);
+    }
+}
+
+// Block-wide barrier that also reports whether any thread raised the local error flag.
+__device__ __forceinline__ bool sync_ok(volatile int *flag) {
+    __syncthreads();
+    return *flag == 0;
+}
+
+template <bool KDA>
+__global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams P) {
+    const RecArgs &a = P.a;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                          ~static_cast<uintptr_t>(1023));
+    float *sf = reinterpret_cast<float *>(sm + SM_SMALL);
+    float *at4 = reinterpret_cast<float *>(sm + SM_AT);
+    uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_SMALL + SF_END * 4);
+    uint64_t *bar_b = bar_a + 1;
+    volatile int *err = reinterpret_cast<volatile int *>(sm + SM_SMALL + SF_END * 4 + 16);
+    volatile int *unit_sh = err + 1;
+    volatile int *slow_sh = err + 2;
+    uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + SM_SMALL + SF_END * 4 + 32);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t lq = tc::tmem_lane_base(warp);  // this warp's TMEM lane quadrant
+    // Two views of the same index: TMEM row (= k-channel c for staging, = v-channel d for the
+    // state phases) and which half of the columns (or of the chunk's rows) this thread takes.
+    const int row = tid & 127;
+    const int half = tid >> 7;
+
+    if (tid == 0) {
+        *err = 0;
+        tc::mbar_init(bar_a, 1);
+        tc::mbar_init(bar_b, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_sh, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = *tmem_sh;
+    uint32_t phase_a = 0, phase_b = 0;
+
+    auto wait_bar = [&](uint64_t *bar, uint32_t &ph) {
+        const bool ok = tc::mbar_wait(bar, ph, WAIT_NS);
+        ph ^= 1u;
+        if (!ok) *err = 1;
+        tc::fence_after_sync();
+    };
+
+    // per-thread column walks (element index fixed per thread)
+    const uint32_t smb = 0;  // offsets are relative to sm
+    ColWalk w_kq, w_kqg, w_v, w_kr;
+    w_kq.init(smb + SM_KQ, row, 128, 2);    // column c of the bf16 K|Q tile
+    w_kqg.init(smb + SM_KQG, row, 128, 4);  // column c of the tf32 Kg|Qg tile
+    w_v.init(smb + SM_V, row, 64, 2);       // column d of the bf16 V tile
+    w_kr.init(smb + SM_KDT, row, 64, 4);    // column c of the tf32 Kr tile (KDA)
+
+    const float scale = a.scale;
+    const int Hv = a.Hv, group = a.Hv / a.Hk;
+    // solver roles: column j, row class p (rows 4m + p)
+    const int sj = 8 * warp + (lane >> 2), sp = lane & 3;
+
+    for (;;) {
+        __syncthreads();  // everyone has read the previous unit index
+        if (tid == 0) *unit_sh = atomicAdd(P.counter, 1);
+        __syncthreads();
+        const int u = *unit_sh;
+        if (u >= P.num_units || *err) break;
+        const int s = P.perm[u / Hv];
+        const int j = u % Hv;
+        const int kh = j / group;
+        int t0, len;
+        if (!stream_range(a.cu, s, a.T_each, a.total, a.max_seqlen, a.status, t0, len)) continue;
+        if (len <= 0) continue;
+        const int nch = (len + TC_C - 1) / TC_C;
+        float *hg = reinterpret_cast<float *>(a.h_ptrs[s]) + (int64_t)j * TC_D * TC_D;
+        __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) + (int64_t)j * TC_D;
+
+        load_kq(a, sm, t0, min(TC_C, len), kh, tid);
+        load_v(a, sm, t0, min(TC_C, len), j, tid);
+        cp_async_commit();
+        // S[d][c] = H[c][d]: thread (d, half) loads columns c in [64*half, 64*half + 64)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = hg[(int64_t)(64 * half + g * 16 + i) * TC_D + row];
+            tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + 64 * half + g * 16), v);
+        }
+        tc::tmem_wait_st();
+
+        for (int ch = 0; ch < nch; ++ch) {
+            const int tok0 = t0 + ch * TC_C;
+            const int n = min(TC_C, len - ch * TC_C);
+            const bool last = (ch + 1 == nch);
+
+            // ---------------- gates
+            float gcr[KDA ? 32 : 1];  // KDA: gc[32*half + t][c], c = row
+            if (KDA) {
+                const float *gp = a.g + ((int64_t)tok0 * Hv + j) * TC_D + row;
+                float acc = 0.f;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int tt = 32 * half + t;
+                    acc += tt < n ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
+                    gcr[t] = acc;
+                }
+                if (half == 0) sf[SF_CARRY + row] = acc;
+                if (tid == 0) *slow_sh = 0;
+            }
+            if (tid < TC_C) {
+                const int t = tid;
+                sf[SF_BETA + t] = t < n ? a.beta[(int64_t)(tok0 + t) * Hv + j] : 0.f;
+                if (!KDA) {
+                    float x = t < n ? a.g[(int64_t)(tok0 + t) * Hv + j] : 0.f;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, off);
+                        if (lane >= off) x += y;
+                    }
+                    if (lane == 31) sf[SF_WARP + warp] = x;
+                    sf[SF_GC + t] = x;  // warp-local; carried below
+                }
+            }
+            cp_async_wait_all();
+            tc::fence_async_smem();
+            if (!sync_ok(err)) break;
+            if (KDA) {
+                if (half == 1) {
+                    const float carry = sf[SF_CARRY + row];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) gcr[t] += carry;
+                    sf[SF_GL + row] = gcr[31];
+                    sf[SF_EL + row] = __expf(gcr[31]);
+                } else {
+                    sf[SF_GM + row] = gcr[31];
+                }
+            } else if (tid < TC_C) {
+                const float gct = sf[SF_GC + tid] + (tid >= 32 ? sf[SF_WARP] : 0.f);
+                sf[SF_GC + tid] = gct;
+                sf[SF_GC2 + tid] = gct * LOG2E;
+            }
+            // pad rows carry pad_fill; every consumer below removes them by select
+            if (n < TC_C && a.pad_fill != 0.f) {
+                const __nv_bfloat16 pf = __float2bfloat16_rn(a.pad_fill);
+                for (int idx = tid; idx < (TC_C - n) * TC_D; idx += TC_THREADS) {
+                    const int r = n + idx / TC_D, c = idx % TC_D;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(r, c, 128, 2)) = pf;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(64 + r, c, 128, 2)) = pf;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + tc::sw128_offset(r, c, 64, 2)) = pf;
+                }
+                tc::fence_async_smem();
+            }
+            __syncthreads();
+            if (!KDA && tid < TC_C) {
+                const float gct = sf[SF_GC + tid], gL = sf[SF_GC + TC_C - 1];
+                sf[SF_EG + tid] = __expf(gct);
+                sf[SF_EGL + tid] = __expf(gL - gct);
+            }
+
+            // ---------------- D1 = [K;Q] K^T (KDA: decays split at row 31)
+            bool slow = false;
+            if (KDA) {
+                const int c = row;
+                const float gm = sf[SF_GM + c];
+                const float gLc = sf[SF_GL + c];
+                if (half == 0 ? (-gm > 80.f) : (gm - gLc > 80.f)) *slow_sh = 1;
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int tt = 32 * half + t;
+                    const float kv = ld_bf16(sm, w_kq.at(tt));
+                    const float qv = ld_bf16(sm, w_kq.at(64 + tt));
+                    const float f1 = __expf(gcr[t] - gm), f2 = __expf(gm - gcr[t]);
+                    st_tf32(sm, w_kqg.at(tt), kv * f1);
+                    st_tf32(sm, w_kqg.at(64 + tt), qv * f1);
+                    st_tf32(sm, w_kr.at(tt), kv * f2);
+                }
+                tc::fence_async_smem();
+                __syncthreads();
+                slow = *slow_sh != 0;
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+            if (!slow && tid == 0) {
+                tc::fence_after_sync();
+                if (KDA) {
+                    constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_TF32);
+#pragma unroll
+                    for (uint32_t kk = 0; kk < 16; ++kk) {
+                        const uint32_t off = (kk & 3u) * 32u;
+                        const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sm + SM_KQG) + (kk >> 2) * 16384u + off);
+                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_KDT) + (kk >> 2) * 8192u + off);
+                        tc::mma_tf32_ss(tm + COL_D1, ad, bd, id, kk > 0);
+                    }
+                } else {
+                    constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_BF16);
+#pragma unroll
+                    for (uint32_t kk = 0; kk < 8; ++kk) {
+                        const uint32_t addr = tc::smem_u32(sm + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u;
+                        tc::mma_bf16_ss(tm + COL_D1, tc::sdesc_sw128(addr), tc::sdesc_sw128(addr), id, kk > 0);
+                    }
+                }
+                tc::mma_commit(bar_a);
+            }
+
+            // ---- staging of the state-MMA operands (thread per (channel c, row half)):
+            //      [K e^gc ; Q e^gc] tf32 [t][c] and (K e^{gc_L - gc})^T tf32 [c][t]
+            auto stage_state_operands = [&]() {
+                const int c = row;
+                const float gLc = KDA ? sf[SF_GL + c] : 0.f;
+                float kd[4];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const int tt = 32 * half + t;
+                    const bool valid = tt < n;
+                    const float kv = ld_bf16(sm, w_kq.at(tt));
+                    const float qv = ld_bf16(sm, w_kq.at(64 + tt));
+                    float eg, egl;
+                    if (KDA) {  // both exponents <= 0 whatever the gates
+                        eg = __expf(gcr[t]);
+                        egl = __expf(gLc - gcr[t]);
+                    } else {
+                        eg = sf[SF_EG + tt];
+                        egl = sf[SF_EGL + tt];
+                    }
+                    st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
+                    st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
+                    kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
+                    if ((t & 3) == 3) {
+                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
+                            make_float4(kd[0], kd[1], kd[2], kd[3]);
+                    }
+                }
+                tc::fence_async_smem();
+            };
+            auto issue_mma2 = [&]() {
+                tc::fence_before_sync();
+                __syncthreads();
+                if (tid == 0) {
+                    tc::fence_after_sync();
+                    constexpr uint32_t id = tc::idesc(128, 128, tc::FMT_TF32);
+#pragma unroll
+                    for (uint32_t kk = 0; kk < 16; ++kk) {
+                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_KQG) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                        tc::mma_tf32_ts(tm + COL_D2, tm + COL_S + kk * 8, bd, id, kk > 0);
+                    }
+                    tc::mma_commit(bar_b);
+                }
+            };
+
+            if (!KDA) {  // GDN: stage while D1 is computed, then start the state MMA
+                stage_state_operands();
+                issue_mma2();
+            }
+
+            // ---------------- D1 ready (or computed exactly on CUDA cores, KDA fallback)
+            if (!slow) {
+                wait_bar(bar_a, phase_a);
+            } else if (KDA) {
+                float *gct = reinterpret_cast<float *>(sm + SM_KQG);  // [64][128] fp32
+                {
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) gct[(32 * half + t) * TC_D + row] = gcr[t];
+                }
+                __syncthreads();
+                if (half == 0) {  // warps 0-3: thread = D1 row
+                    const int r = row & 63;
+                    const bool isq = row >= 64;
+                    for (int g = 0; g < 4; ++g) {
+                        float v[16];
+                        for (int ii = 0; ii < 16; ++ii) {
+                            const int i = g * 16 + ii;
+                            float acc = 0.f;
+                            if (i <= r) {
+                                for (int c = 0; c < TC_D; ++c) {
+                                    const float lv = ld_bf16(sm, SM_KQ + tc::sw128_offset((isq ? 64 : 0) + r, c, 128, 2));
+                                    const float kv = ld_bf16(sm, SM_KQ + tc::sw128_offset(i, c, 128, 2));
+                                    acc = fmaf(lv * kv, __expf(gct[r * TC_D + c] - gct[i * TC_D + c]), acc);
+                                }
+                            }
+                            v[ii] = acc;
+                        }
+                        tc::tmem_st16(tc::tmem_addr(tm, lq, COL_D1 + g * 16), v);
+                    }
+                    tc::tmem_wait_st();
+                }
+                tc::fence_before_sync();
+                __syncthreads();
+                tc::fence_after_sync();
+            }
+            if (!sync_ok(err)) break;
+
+            // ---------------- A^T (fp32, split by row class) and P (tf32) from D1
+            {
+                const int r = row & 63;
+                const bool isq = row >= 64;
+                const float gct2 = KDA ? 0.f : sf[SF_GC2 + r];
+                const float bt = sf[SF_BETA + r];
+                const bool rv = r < n;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int i0 = 32 * half + 16 * g;
+                    float v[16];
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D1 + i0), v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int ii = 0; ii < 16; ++ii) {
+                        const int i = i0 + ii;
+                        const float dec = KDA ? 1.f : exp2f(gct2 - sf[SF_GC2 + i]);
+                        v[ii] = isq ? ((rv && i <= r) ? dec * v[ii] : 0.f)
+                                    : ((rv && i < r) ? bt * dec * v[ii] : 0.f);
+                    }
+                    if (isq) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<float4 *>(sm + SM_P + tc::sw128_offset(r, i0 + q4 * 4, 64, 4)) =
+                                make_float4(tc::to_tf32(v[q4 * 4]), tc::to_tf32(v[q4 * 4 + 1]),
+                                            tc::to_tf32(v[q4 * 4 + 2]), tc::to_tf32(v[q4 * 4 + 3]));
+                    } else {
+#pragma unroll
+                        for (int ii = 0; ii < 16; ++ii)
+                            at4[(i0 + ii) * AT_I + (r & 3) * AT_P + (r >> 2)] = v[ii];
+                    }
+                }
+            }
+            tc::fence_async_smem();
+            __syncthreads();
+
+            if (KDA) {  // KDA: the Kl|Ql and Kr buffers are free now
+                stage_state_operands();
+                issue_mma2();
+            }
+
+            // ---------------- T = (I + A)^{-1}: 4 threads per column j, rows 4m + p
+            {
+                float x[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) x[m] = (4 * m + sp == sj) ? 1.f : 0.f;
+                const float *atp = at4 + sp * AT_P;
+#pragma unroll
+                for (int i = 0; i < TC_C - 1; ++i) {
+                    const int m0 = i >> 2;
+                    const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~3) | (i & 3));
+                    {
+                        const float nx = fmaf(-atp[i * AT_I + m0], xi, x[m0]);
+                        x[m0] = (sp > (i & 3)) ? nx : x[m0];
+                    }
+#pragma unroll
+                    for (int m = m0 + 1; m < 16; ++m) x[m] = fmaf(-atp[i * AT_I + m], xi, x[m]);
+                }
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    st_tf32(sm, SM_T + tc::sw128_offset(4 * m + sp, sj, 64, 4), x[m]);
+            }
+            tc::fence_async_smem();
+            __syncthreads();
+            if (!last) {  // K|Q tile is free: next chunk's K, Q in flight
+                load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+                cp_async_commit();
+            }
+
+            // ---------------- D2 ready: R^T = beta (V^T - D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})
+            wait_bar(bar_b, phase_b);
+            if (!sync_ok(err)) break;
+            {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int t0c = 32 * half + 16 * g;
+                    float v[16];
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + t0c), v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int ii = 0; ii < 16; ++ii) {
+                        const int t = t0c + ii;
+                        const float vv = ld_bf16(sm, w_v.at(t));
+                        v[ii] = t < n ? tc::to_tf32(sf[SF_BETA + t] * (vv - v[ii])) : 0.f;
+                    }
+                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                }
+                const float egL = KDA ? 0.f : sf[SF_EG + TC_C - 1];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int c0 = 64 * half + 16 * g;
+                    float v[16];
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + c0), v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int ii = 0; ii < 16; ++ii) v[ii] *= KDA ? sf[SF_EL + c0 + ii] : egL;
+                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0), v);
+                }
+                tc::tmem_wait_st();
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+
+            // ---------------- U'^T = R^T T^T ; next chunk's V in flight
+            if (tid == 0) {
+                tc::fence_after_sync();
+                constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_TF32);
+#pragma unroll
+                for (uint32_t kk = 0; kk < 8; ++kk) {
+                    const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_T) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
+                    tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8, bd, id, kk > 0);
+                }
+                tc::mma_commit(bar_b);
+            }
+            if (!last) {
+                load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid);
+                cp_async_commit();
+            }
+            wait_bar(bar_b, phase_b);
+            if (!sync_ok(err)) break;
+
+            // ---------------- U'^T rounded to tf32 -> TMEM (A operand of the next two MMAs)
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int t0c = 32 * half + 16 * g;
+                float v[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) v[ii] = tc::to_tf32(v[ii]);
+                tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncthreads();
+
+            // ---------------- O^T += U'^T P^T ; S += U'^T Kdec
+            if (tid == 0) {
+                tc::fence_after_sync();
+                constexpr uint32_t id64 = tc::idesc(128, 64, tc::FMT_TF32);
+                constexpr uint32_t id128 = tc::idesc(128, 128, tc::FMT_TF32);
+#pragma unroll
+                for (uint32_t kk = 0; kk < 8; ++kk) {
+                    const uint64_t bp = tc::sdesc_sw128(tc::smem_u32(sm + SM_P) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
+                    tc::mma_tf32_ts(tm + COL_D2 + 64, tm + COL_RU + kk * 8, bp, id64, 1);
+                }
+#pragma unroll
+                for (uint32_t kk = 0; kk < 8; ++kk) {
+                    const uint64_t bk = tc::sdesc_sw128(tc::smem_u32(sm + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                    tc::mma_tf32_ts(tm + COL_S, tm + COL_RU + kk * 8, bk, id128, 1);
+                }
+                tc::mma_commit(bar_b);
+            }
+            wait_bar(bar_b, phase_b);
+            if (!sync_ok(err)) break;
+
+            // ---------------- o = scale O, rows < n
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int t0c = 32 * half + 16 * g;
+                float v[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) {
+                    const int t = t0c + ii;
+                    if (t < n) og[(int64_t)(tok0 + t) * Hv * TC_D + row] = __float2bfloat16_rn(scale * v[ii]);
+                }
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+            tc::fence_after_sync();
+        }
+        if (*err) break;
+
+        // state back: H[c][d] = S[d][c]
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            float v[16];
+            tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + 64 * half + g * 16), v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) hg[(int64_t)(64 * half + g * 16 + i) * TC_D + row] = v[i];
+        }
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+
+    cp_async_wait_all();
+    if (*err && tid == 0) raise_status(a.status, LA_DEV_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
+}
+
+// Orders the streams by decreasing length (stable) so that the longest units start first,
+// and zeroes the unit counter. One block; B <= 1024 per pass of the rank computation.
+__global__ void order_streams_kernel(const int32_t *cu, int B, int T_each, int32_t *perm,
+                                     int *counter) {
+    for (int s = threadIdx.x; s < B; s += blockDim.x) {
+        const int ls = cu ? cu[s + 1] - cu[s] : T_each;
+        int rank = 0;
+        for (int o = 0; o < B; ++o) {
+            const int lo = cu ? cu[o + 1] - cu[o] : T_each;
+            rank += (lo > ls) || (lo == ls && o < s);
+        }
+        perm[rank] = s;
+    }
+    if (threadIdx.x == 0) *counter = 0;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+}  // namespace
+
+size_t chunk_tc_workspace_bytes(int B) {
+    return (size_t)((B + 64 + 63) / 64) * 64 * sizeof(int32_t) + 256;
+}
+
+bool chunk_tc_supported(const RecArgs &a) {
+    return a.dtype == LA_BF16 && a.dk == TC_D && a.dv == TC_D;
+}
+
+cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st) {
+    int32_t *perm = reinterpret_cast<int32_t *>(a.workspace);
+    int *counter = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(a.workspace) +
+                                           chunk_tc_workspace_bytes(a.B) - 256);
+    order_streams_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.T_each, perm, counter);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    TcParams P;
+    P.a = a;
+    P.perm = perm;
+    P.counter = counter;
+    P.num_units = a.B * a.Hv;
+    const int grid = min(P.num_units, sm_count());
+    auto kern = a.kda ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, TC_THREADS, TC_SMEM, st>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace la

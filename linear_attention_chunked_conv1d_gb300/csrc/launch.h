@@ -45,7 +45,13 @@ struct RecArgs {
     size_t workspace_bytes;
     int *status;
 };
-// CUDA-core chunked kernel (fp32 and bf16 activations).
+// CUDA-core chunked kernel (fp32 and bf16 activations, head dims 64 and 128).
 cudaError_t launch_chunk_simt(const RecArgs &a, cudaStream_t st);
+
+// Tensor-core (tcgen05) chunked kernel: bf16 activations, dk = dv = 128. Needs a workspace of
+// chunk_tc_workspace_bytes(B) bytes (stream order + unit counter).
+bool chunk_tc_supported(const RecArgs &a);
+size_t chunk_tc_workspace_bytes(int B);
+cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st);
 
 }  // namespace la

@@ -113,16 +113,18 @@ def run_rec(cuda, inp, Hk, Hv, d, *, kda, mode, pad_fill=0.0, scale=None, guard=
     ptrs = la.pointer_array([h[s] for s in range(B)])
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     cu = inp["cu_seqlens"].to(cuda)
+    nbytes = la.prefill_workspace_bytes(B, T, Hk, Hv, d, d, q.dtype)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=cuda) if nbytes else None
     if kda:
         la.kda_prefill(ptrs, q, k, v, g, beta, out, None if mode == "single" else cu,
                        Hk=Hk, Hv=Hv, dk=d, dv=d, max_seqlen=max(lengths), scale=scale,
-                       pad_fill=pad_fill)
+                       pad_fill=pad_fill, workspace=ws)
     elif mode == "batched":
         la.gdn_prefill_batched(ptrs, q, k, v, g, beta, out, B=B, T=lengths[0], Hk=Hk, Hv=Hv,
-                               dk=d, dv=d, scale=scale)
+                               dk=d, dv=d, scale=scale, workspace=ws)
     else:
         la.gdn_prefill_varlen(ptrs, q, k, v, g, beta, out, cu, max_seqlen=max(lengths), Hk=Hk,
-                              Hv=Hv, dk=d, dv=d, scale=scale)
+                              Hv=Hv, dk=d, dv=d, scale=scale, workspace=ws)
     torch.cuda.synchronize()
     assert la.device_status() == 0
     if guard:
@@ -196,8 +198,10 @@ def test_pad_rows_in_caller_buffers_ignored(cuda):
     gd, bd = padded["g"].to(cuda), padded["beta"].to(cuda)
     h = inp["h"].clone().to(cuda)
     out = torch.empty(T, Hv, d, dtype=torch.bfloat16, device=cuda)
+    ws = torch.empty(la.prefill_workspace_bytes(1, T, Hk, Hv, d, d, la.LA_BF16),
+                     dtype=torch.uint8, device=cuda)
     la.kda_prefill(la.pointer_array([h[0]]), qd, kd, vd, gd, bd, out, None, Hk=Hk, Hv=Hv, dk=d,
-                   dv=d, total_tokens=T)
+                   dv=d, total_tokens=T, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(out.cpu(), base[0]) and torch.equal(h.cpu(), base[1])
 
@@ -262,3 +266,43 @@ def test_refusal_leaves_buffers_untouched(cuda):
     assert ei.value.code == la.LA_ERR_COUNT
     torch.cuda.synchronize()
     assert torch.all(out.cpu() == 5.0) and torch.equal(h.cpu(), inp["h"])
+
+
+def test_kda_extreme_gates_exact_path(cuda):
+    """Half-chunk decays beyond e^80 in some channels: the tensor-core kernel must take its exact
+    pairwise-exponent path for those chunks and still match the oracle."""
+    inp = recurrence_inputs([150], 2, 2, 128, kda=True, dtype="bf16", seed=91)
+    g = inp["g"].clone()
+    g[:, :, :8] = -12.0          # 8 channels decay by e^-12 per token
+    g[40:60, 1, 100:] = -30.0    # and a burst on another head
+    inp["g"] = g
+    o, h = run_rec(cuda, inp, 2, 2, 128, kda=True, mode="single")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(h).all()
+    check_parity(inp, o, h, 2, 2, 128, True, "bf16")
+
+
+def test_bad_cu_seqlens_tensor_core_path(cuda):
+    inp = recurrence_inputs([50, 50], 1, 1, 128, dtype="bf16", seed=43)
+    T = 100
+    q, k, v = (inp[n].to(cuda).reshape(T, -1) for n in ("q", "k", "v"))
+    h = inp["h"].clone().to(cuda)
+    out = torch.zeros(T, 1, 128, dtype=torch.bfloat16, device=cuda)
+    ws = torch.empty(la.prefill_workspace_bytes(2, T, 1, 1, 128, 128, la.LA_BF16),
+                     dtype=torch.uint8, device=cuda)
+    bad = torch.tensor([0, 70, 60], dtype=torch.int32, device=cuda)
+    la.device_status()
+    la.gdn_prefill_varlen(la.pointer_array([h[0], h[1]]), q, k, v, inp["g"].to(cuda),
+                          inp["beta"].to(cuda), out, bad, max_seqlen=70, Hk=1, Hv=1, dk=128,
+                          dv=128, total_tokens=T, workspace=ws)
+    assert la.device_status() & la.LA_DEV_BAD_SEQLENS
+
+
+def test_workspace_too_small_is_refused(cuda):
+    inp = recurrence_inputs([64], 1, 1, 128, dtype="bf16", seed=44)
+    q, k, v = (inp[n].to(cuda).reshape(64, -1) for n in ("q", "k", "v"))
+    h = inp["h"].clone().to(cuda)
+    out = torch.zeros(64, 1, 128, dtype=torch.bfloat16, device=cuda)
+    with pytest.raises(la.LinAttnError) as ei:
+        la.gdn_prefill_batched(la.pointer_array([h[0]]), q, k, v, inp["g"].to(cuda),
+                               inp["beta"].to(cuda), out, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128)
+    assert ei.value.code == la.LA_ERR_ARG
