@@ -156,10 +156,10 @@ int la_gdn_prefill_varlen(const uint64_t *h_state_ptrs, const void *q, const voi
 /* KDA (per-channel gate) over one stream (cu_seqlens == NULL: tokens 0..total_tokens-1, B = 1)
  * or B varlen streams. "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill.
  * gate [total_tokens][Hv][dk] fp32 log-decay per k-channel.
- * pad_fill: the value the kernels place in q/k/v tile rows at or past a stream's end before
+ * pad_fill: the value the kernels place in the q/k tile rows at or past a stream's end before
  *   masking them (the pages fill the padded q/k/v tails with it). Outputs and states do not
- *   depend on it: positions past the end are ignored in-kernel, by select, never by a zero
- *   multiply, so NaN works too.
+ *   depend on it: positions past the end are removed in-kernel by select, never by a zero
+ *   multiply, so NaN works too. Tiles that a kernel contracts over tokens keep zeros there.
  * Count rule: 1 <= total_tokens <= max_tokens. */
 int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, const void *v,
                    const float *gate, const float *beta, void *out, const int32_t *cu_seqlens,

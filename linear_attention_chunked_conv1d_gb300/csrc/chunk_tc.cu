@@ -42,18 +42,22 @@ constexpr int TC_D = 128;        // dk = dv
 constexpr int TC_THREADS = 256;  // 8 warps: warp w owns TMEM lanes 32*(w%4).. and column half w/4
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-// TMEM columns
-constexpr uint32_t COL_S = 0, COL_D2 = 128, COL_RU = 256, COL_D6 = 320, COL_D1 = 384;
+// TMEM columns. D1 (K K^T | Q K^T) and D6 (U'^T) share columns: D1 is consumed before D6 is
+// produced. V^T (identity MMA) lands in the U'd^T columns before they are reused; K^T (identity
+// MMA, GDN) lands in the P U' accumulator columns before MMA4 overwrites them.
+constexpr uint32_t COL_S = 0, COL_D2 = 128, COL_RU = 256, COL_RUD = 320, COL_D1 = 384,
+                   COL_D6 = 384, COL_D4 = 448;
 constexpr uint32_t TMEM_COLS = 512;
 
 // shared memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t SM_KQ = 0;                    // bf16 SW128 [128 rows: K | Q][128]
 constexpr uint32_t SM_V = SM_KQ + 32768;         // bf16 SW128 [64][128]
-constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: Kg | Qg][128]; KDA: Kl|Ql
-constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t] (Kdec^T); KDA: Kr
+constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: K | Q][128] (KDA: scaled)
+constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t]: K^T (GDN) / Kdec^T (KDA)
 constexpr uint32_t SM_P = SM_KDT + 32768;        // tf32 SW128 [64 t][64 i]
 constexpr uint32_t SM_T = SM_P + 16384;          // tf32 SW128 [64 t][64 i]
-constexpr uint32_t SM_AT = SM_T + 16384;         // fp32 A^T split by row parity: [64 i][4][20]
+constexpr uint32_t SM_ID = SM_T + 16384;         // bf16 SW128 [64][64] identity
+constexpr uint32_t SM_AT = SM_ID + 8192;         // fp32 A^T split by row class: [64 i][4][20]
 constexpr uint32_t AT_I = 80, AT_P = 20;         // floats per i row / per row class
 constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_I * 4;
 // small region (floats)
@@ -161,8 +165,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t lq = tc::tmem_lane_base(warp);  // this warp's TMEM lane quadrant
-    // Two views of the same index: TMEM row (= k-channel c for staging, = v-channel d for the
-    // state phases) and which half of the columns (or of the chunk's rows) this thread takes.
+    // TMEM row (= k-channel c when staging, = v-channel d in the state phases) and the half of
+    // the columns (or of the chunk's rows) this thread takes.
     const int row = tid & 127;
     const int half = tid >> 7;
 
@@ -172,6 +176,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         tc::mbar_init(bar_b, 1);
         tc::fence_mbar_init();
     }
+    // identity tile (bf16, K-major 64x64) for the transposing MMAs
+    for (int idx = tid; idx < 64 * 64; idx += TC_THREADS) {
+        const int r = idx >> 6, k = idx & 63;
+        *reinterpret_cast<__nv_bfloat16 *>(sm + SM_ID + tc::sw128_offset(r, k, 64, 2)) =
+            __float2bfloat16_rn(r == k ? 1.f : 0.f);
+    }
+    tc::fence_async_smem();
     if (warp == 0) {
         tc::tmem_alloc(tmem_sh, TMEM_COLS);
         tc::tmem_relinquish();
@@ -189,18 +200,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         tc::fence_after_sync();
     };
 
-    // per-thread column walks (element index fixed per thread)
-    const uint32_t smb = 0;  // offsets are relative to sm
-    ColWalk w_kq, w_kqg, w_v, w_kr;
-    w_kq.init(smb + SM_KQ, row, 128, 2);    // column c of the bf16 K|Q tile
-    w_kqg.init(smb + SM_KQG, row, 128, 4);  // column c of the tf32 Kg|Qg tile
-    w_v.init(smb + SM_V, row, 64, 2);       // column d of the bf16 V tile
-    w_kr.init(smb + SM_KDT, row, 64, 4);    // column c of the tf32 Kr tile (KDA)
+    ColWalk w_kq, w_kqg, w_kr;
+    w_kq.init(SM_KQ, row, 128, 2);    // column c of the bf16 K|Q tile
+    w_kqg.init(SM_KQG, row, 128, 4);  // column c of the tf32 K|Q tile
+    w_kr.init(SM_KDT, row, 64, 4);    // column c of the tf32 Kr tile (KDA)
 
     const float scale = a.scale;
     const int Hv = a.Hv, group = a.Hv / a.Hk;
-    // solver roles: column j, row class p (rows 4m + p)
-    const int sj = 8 * warp + (lane >> 2), sp = lane & 3;
+    const int sj = 8 * warp + (lane >> 2), sp = lane & 3;  // solver: column j, rows 4m + p
 
     for (;;) {
         __syncthreads();  // everyone has read the previous unit index
@@ -282,14 +289,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 sf[SF_GC + tid] = gct;
                 sf[SF_GC2 + tid] = gct * LOG2E;
             }
-            // pad rows carry pad_fill; every consumer below removes them by select
+            // Pad rows of the K|Q tile carry pad_fill; every consumer removes them by select.
+            // (The V tile keeps the zeros of the async copy: it is contracted over tokens by
+            // the transposing MMA, where a NaN row would reach every column even through an
+            // exact zero weight.)
             if (n < TC_C && a.pad_fill != 0.f) {
                 const __nv_bfloat16 pf = __float2bfloat16_rn(a.pad_fill);
                 for (int idx = tid; idx < (TC_C - n) * TC_D; idx += TC_THREADS) {
                     const int r = n + idx / TC_D, c = idx % TC_D;
                     *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(r, c, 128, 2)) = pf;
                     *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(64 + r, c, 128, 2)) = pf;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + tc::sw128_offset(r, c, 64, 2)) = pf;
                 }
                 tc::fence_async_smem();
             }
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 sf[SF_EGL + tid] = __expf(gL - gct);
             }
 
-            // ---------------- D1 = [K;Q] K^T (KDA: decays split at row 31)
+            // ---------------- D1 = [K;Q] K^T (KDA: decays split at row 31); GDN also K^T
             bool slow = false;
             if (KDA) {
                 const int c = row;
@@ -341,40 +350,63 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                         const uint32_t addr = tc::smem_u32(sm + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u;
                         tc::mma_bf16_ss(tm + COL_D1, tc::sdesc_sw128(addr), tc::sdesc_sw128(addr), id, kk > 0);
                     }
+                    // K^T[c][t] = sum_i K[i][c] I[t][i]: A = K tile read MN-major
+                    constexpr uint32_t idt = tc::idesc(128, 64, tc::FMT_BF16, true, false);
+#pragma unroll
+                    for (uint32_t kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = tc::sdesc_sw128_mn(tc::smem_u32(sm + SM_KQ) + kk * 2048u, 128u * 128u, 1024u);
+                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_ID) + kk * 32u);
+                        tc::mma_bf16_ss(tm + COL_D4, ad, bd, idt, kk > 0);
+                    }
                 }
                 tc::mma_commit(bar_a);
             }
 
-            // ---- staging of the state-MMA operands (thread per (channel c, row half)):
-            //      [K e^gc ; Q e^gc] tf32 [t][c] and (K e^{gc_L - gc})^T tf32 [c][t]
+            // ---- state-MMA operands. GDN: exact tf32 copy of [K;Q] (the gate factors are
+            //      applied to the MMA results instead). KDA: [K e^gc ; Q e^gc] and
+            //      (K e^{gc_L - gc})^T, thread per (channel, row half).
             auto stage_state_operands = [&]() {
-                const int c = row;
-                const float gLc = KDA ? sf[SF_GL + c] : 0.f;
-                float kd[4];
+                if (!KDA) {
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int tt = 32 * half + t;
-                    const bool valid = tt < n;
-                    const float kv = ld_bf16(sm, w_kq.at(tt));
-                    const float qv = ld_bf16(sm, w_kq.at(64 + tt));
-                    float eg, egl;
-                    if (KDA) {  // both exponents <= 0 whatever the gates
-                        eg = __expf(gcr[t]);
-                        egl = __expf(gLc - gcr[t]);
-                    } else {
-                        eg = sf[SF_EG + tt];
-                        egl = sf[SF_EGL + tt];
+                    for (int m = 0; m < 8; ++m) {
+                        const int idx = tid + TC_THREADS * m;  // 0..2047 chunks of 8 elements
+                        const int r = idx >> 4, cj = idx & 15;
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
+                        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            f[2 * e] = __uint_as_float(w4[e] << 16);
+                            f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+                        }
+                        *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8, 128, 4)) =
+                            make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8 + 4, 128, 4)) =
+                            make_float4(f[4], f[5], f[6], f[7]);
                     }
-                    st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
-                    st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
-                    kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
-                    if ((t & 3) == 3) {
-                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
-                            make_float4(kd[0], kd[1], kd[2], kd[3]);
+                } else {
+                    const int c = row;
+                    const float gLc = sf[SF_GL + c];
+                    float kd[4];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int tt = 32 * half + t;
+                        const bool valid = tt < n;
+                        const float kv = ld_bf16(sm, w_kq.at(tt));
+                        const float qv = ld_bf16(sm, w_kq.at(64 + tt));
+                        const float eg = __expf(gcr[t]), egl = __expf(gLc - gcr[t]);  // both <= 1
+                        st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
+                        st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
+                        kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
+                        if ((t & 3) == 3) {
+                            *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
+                                make_float4(kd[0], kd[1], kd[2], kd[3]);
+                        }
                     }
                 }
                 tc::fence_async_smem();
             };
+            // D2 = S [K;Q]^T (tf32, A from TMEM) and V^T (identity MMA) into the U'd columns
             auto issue_mma2 = [&]() {
                 tc::fence_before_sync();
                 __syncthreads();
@@ -386,11 +418,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                         const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_KQG) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
                         tc::mma_tf32_ts(tm + COL_D2, tm + COL_S + kk * 8, bd, id, kk > 0);
                     }
+                    constexpr uint32_t idv = tc::idesc(128, 64, tc::FMT_BF16, true, false);
+#pragma unroll
+                    for (uint32_t kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = tc::sdesc_sw128_mn(tc::smem_u32(sm + SM_V) + kk * 2048u, 64u * 128u, 1024u);
+                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_ID) + kk * 32u);
+                        tc::mma_bf16_ss(tm + COL_RUD, ad, bd, idv, kk > 0);
+                    }
                     tc::mma_commit(bar_b);
                 }
             };
 
-            if (!KDA) {  // GDN: stage while D1 is computed, then start the state MMA
+            if (!KDA) {  // GDN: stage while D1 and K^T are computed, then start the state MMA
                 stage_state_operands();
                 issue_mma2();
             }
@@ -400,10 +439,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 wait_bar(bar_a, phase_a);
             } else if (KDA) {
                 float *gct = reinterpret_cast<float *>(sm + SM_KQG);  // [64][128] fp32
-                {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) gct[(32 * half + t) * TC_D + row] = gcr[t];
-                }
+                for (int t = 0; t < 32; ++t) gct[(32 * half + t) * TC_D + row] = gcr[t];
                 __syncthreads();
                 if (half == 0) {  // warps 0-3: thread = D1 row
                     const int r = row & 63;
@@ -432,7 +469,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
             if (!sync_ok(err)) break;
 
-            // ---------------- A^T (fp32, split by row class) and P (tf32) from D1
+            // ---------------- A^T (fp32, split by row class) and P (tf32) from D1; GDN: K^T tile
             {
                 const int r = row & 63;
                 const bool isq = row >= 64;
@@ -462,6 +499,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 #pragma unroll
                         for (int ii = 0; ii < 16; ++ii)
                             at4[(i0 + ii) * AT_I + (r & 3) * AT_P + (r >> 2)] = v[ii];
+                    }
+                }
+                if (!KDA) {
+                    // K^T[c][t] (exact in tf32) -> the [c][t] tile; columns t >= n zeroed
+                    const int c = row;
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        const int t0c = 32 * half + 16 * g;
+                        float v[16];
+                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), v);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int t = t0c + q4 * 4;
+                            *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, t, 128, 4)) =
+                                make_float4(t + 0 < n ? v[q4 * 4 + 0] : 0.f, t + 1 < n ? v[q4 * 4 + 1] : 0.f,
+                                            t + 2 < n ? v[q4 * 4 + 2] : 0.f, t + 3 < n ? v[q4 * 4 + 3] : 0.f);
+                        }
                     }
                 }
             }
@@ -501,21 +556,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 cp_async_commit();
             }
 
-            // ---------------- D2 ready: R^T = beta (V^T - D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})
+            // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
+            if (!last) {  // V tile consumed by the identity MMA: next chunk's V in flight
+                load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid);
+                cp_async_commit();
+            }
             {
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int t0c = 32 * half + 16 * g;
-                    float v[16];
+                    float v[16], vt[16];
                     tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + t0c), v);
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RUD + t0c), vt);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int ii = 0; ii < 16; ++ii) {
                         const int t = t0c + ii;
-                        const float vv = ld_bf16(sm, w_v.at(t));
-                        v[ii] = t < n ? tc::to_tf32(sf[SF_BETA + t] * (vv - v[ii])) : 0.f;
+                        const float kh_t = KDA ? v[ii] : sf[SF_EG + t] * v[ii];
+                        v[ii] = t < n ? tc::to_tf32(sf[SF_BETA + t] * (vt[ii] - kh_t)) : 0.f;
                     }
                     tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
                 }
@@ -535,7 +595,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             tc::fence_before_sync();
             __syncthreads();
 
-            // ---------------- U'^T = R^T T^T ; next chunk's V in flight
+            // ---------------- U'^T = R^T T^T
             if (tid == 0) {
                 tc::fence_after_sync();
                 constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_TF32);
@@ -546,29 +606,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
                 tc::mma_commit(bar_b);
             }
-            if (!last) {
-                load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid);
-                cp_async_commit();
-            }
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
 
-            // ---------------- U'^T rounded to tf32 -> TMEM (A operand of the next two MMAs)
+            // ------ U'^T -> TMEM (tf32); GDN also U'^T diag(e^{gc_L - gc}) for the state update
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 const int t0c = 32 * half + 16 * g;
                 float v[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);
                 tc::tmem_wait_ld();
+                float w[16];
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) v[ii] = tc::to_tf32(v[ii]);
+                for (int ii = 0; ii < 16; ++ii) {
+                    w[ii] = KDA ? 0.f : tc::to_tf32(v[ii] * sf[SF_EGL + t0c + ii]);
+                    v[ii] = tc::to_tf32(v[ii]);
+                }
                 tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                if (!KDA) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RUD + t0c), w);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncthreads();
 
-            // ---------------- O^T += U'^T P^T ; S += U'^T Kdec
+            // ---------------- D4 = U'^T P^T ; S += U'd^T K (GDN) or U'^T Kdec (KDA)
             if (tid == 0) {
                 tc::fence_after_sync();
                 constexpr uint32_t id64 = tc::idesc(128, 64, tc::FMT_TF32);
@@ -576,29 +637,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
                     const uint64_t bp = tc::sdesc_sw128(tc::smem_u32(sm + SM_P) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
-                    tc::mma_tf32_ts(tm + COL_D2 + 64, tm + COL_RU + kk * 8, bp, id64, 1);
+                    tc::mma_tf32_ts(tm + COL_D4, tm + COL_RU + kk * 8, bp, id64, kk > 0);
                 }
+                const uint32_t a5 = KDA ? COL_RU : COL_RUD;
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
                     const uint64_t bk = tc::sdesc_sw128(tc::smem_u32(sm + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
-                    tc::mma_tf32_ts(tm + COL_S, tm + COL_RU + kk * 8, bk, id128, 1);
+                    tc::mma_tf32_ts(tm + COL_S, tm + a5 + kk * 8, bk, id128, 1);
                 }
                 tc::mma_commit(bar_b);
             }
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
 
-            // ---------------- o = scale O, rows < n
+            // ---------------- o = scale (e^gc (Q H) + P U'), rows < n
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
                 const int t0c = 32 * half + 16 * g;
-                float v[16];
-                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), v);
+                float vq[16], vp[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
                     const int t = t0c + ii;
-                    if (t < n) og[(int64_t)(tok0 + t) * Hv * TC_D + row] = __float2bfloat16_rn(scale * v[ii]);
+                    const float o = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
+                    if (t < n) og[(int64_t)(tok0 + t) * Hv * TC_D + row] = __float2bfloat16_rn(scale * o);
                 }
             }
             tc::fence_before_sync();

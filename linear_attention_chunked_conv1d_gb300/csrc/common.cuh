@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/linattn.h"
+#include "linattn.h"
 
 namespace la {
 

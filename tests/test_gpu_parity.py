@@ -139,6 +139,8 @@ def check_parity(inp, got_out, got_h, Hk, Hv, d, kda, dtype):
     tol = TOL[dtype]
     e_out = max_abs(f64(got_out), ref_out)
     e_h = rel_frob(f64(got_h), ref_h)
+    print(f"\n[parity] {dtype} d={d} kda={kda}: max|o-o_ref| = {e_out:.3e}, "
+          f"state rel.Frobenius = {e_h:.3e}")
     assert e_out <= tol["out"], f"max |o - o_ref| = {e_out:.3g} > {tol['out']}"
     assert e_h <= tol["state"], f"state rel. Frobenius error {e_h:.3g} > {tol['state']}"
     return e_out, e_h

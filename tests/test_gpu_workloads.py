@@ -54,6 +54,8 @@ def check_workload(wl, cuda, pad_fill=0.0, seed=0):
         worst_o = max(worst_o, max_abs(got_o, ref_o))
         worst_h = max(worst_h, rel_frob(got_h, ref_h[0]))
     tol = TOL[act]
+    print(f"\n[parity] {wl.name}: max|o-o_ref| = {worst_o:.3e} (bar {tol['out']:.0e}), "
+          f"state rel.Frobenius = {worst_h:.3e} (bar {tol['state']:.0e})")
     assert worst_o <= tol["out"], f"{wl.name}: max |o - o_ref| = {worst_o:.3g}"
     assert worst_h <= tol["state"], f"{wl.name}: state rel. Frobenius error {worst_h:.3g}"
     return p
