@@ -101,6 +101,20 @@ int la_conv1d_silu_prefill_varlen(const uint64_t *conv_state_ptrs, const void *x
                                   int64_t x_stride, int64_t out_stride, int dtype,
                                   uint64_t stream);
 
+/* Fused front end: conv1d + SiLU as above (single stream when cu_seqlens is NULL and B == 1,
+ * else varlen), then the per-(token, head) L2 norm of la_l2norm_heads over the first
+ * l2_heads*head_dim output channels, in one pass: x is read once and out written once. The conv
+ * output is rounded to dtype before it is normalised, exactly as the two separate calls store
+ * and re-read it, so the results are bitwise identical to la_conv1d_silu_prefill[_varlen]
+ * followed by la_l2norm_heads ("glm5next_kda/prefill.rs": conv_prefill then l2 on conv_out).
+ * conv_state_ptrs: DEVICE array of B device pointers to [kernel-1][channels] states.
+ * head_dim in {64, 128}; l2_heads*head_dim <= channels. */
+int la_conv1d_silu_l2_prefill(const uint64_t *conv_state_ptrs, const void *x, const void *w,
+                              const void *bias, void *out, const int32_t *cu_seqlens, int B,
+                              int total_tokens, int max_tokens, int channels, int kernel,
+                              int l2_heads, int head_dim, float eps, int64_t x_stride,
+                              int64_t out_stride, int dtype, uint64_t stream);
+
 /* ---------------------------------------------------------------------------------------------
  * Per-(token, head) L2 norm, in place, over the first n_heads*head_dim channels of each row.
  * "glm5next_kda/prefill.rs", l2 launch (grid q|k heads x tokens, eps = cfg.l2_eps);

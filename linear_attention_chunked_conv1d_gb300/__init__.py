@@ -18,7 +18,8 @@ from .build import LIB_PATH
 
 __all__ = [
     "LinAttnError", "LA_F32", "LA_BF16", "abi_version", "last_error", "device_status",
-    "conv1d_silu_prefill", "conv1d_silu_prefill_varlen", "l2norm_heads",
+    "conv1d_silu_prefill", "conv1d_silu_prefill_varlen", "conv1d_silu_l2_prefill",
+    "l2norm_heads",
     "prefill_workspace_bytes", "gdn_prefill_batched", "gdn_prefill_varlen", "kda_prefill",
     "pointer_array", "library_path",
 ]
@@ -50,6 +51,8 @@ _SIGS = {
     "la_conv1d_silu_prefill_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                        _i32, _i64, _i64, _i32, _u64], ctypes.c_int),
     "la_l2norm_heads": ([_vp, _i32, _i32, _i32, _i64, _f32, _i32, _u64], ctypes.c_int),
+    "la_conv1d_silu_l2_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                                   _i32, _i32, _f32, _i64, _i64, _i32, _u64], ctypes.c_int),
     "la_prefill_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32, _i32], _sz),
     "la_gdn_prefill_batched": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                                 _i32, _i32, _i64, _i64, _i64, _f32, _i32, _vp, _sz, _u64],
@@ -156,6 +159,19 @@ def conv1d_silu_prefill_varlen(conv_state_ptrs, x, w, out, cu_seqlens, *, bias=N
         _ptr(conv_state_ptrs), _ptr(x), _ptr(w), _ptr(bias), _ptr(out), _ptr(cu_seqlens), B,
         total, max_tokens if max_tokens is not None else total, C, K, _row_stride(x),
         _row_stride(out), _dtype_code(x), _stream(stream)))
+
+
+def conv1d_silu_l2_prefill(conv_state_ptrs, x, w, out, cu_seqlens=None, *, l2_heads, head_dim,
+                           eps=1e-6, bias=None, total_tokens=None, max_tokens=None,
+                           stream=None) -> None:
+    """Fused conv1d + SiLU + per-head L2 over the first l2_heads*head_dim channels (one pass)."""
+    B = 1 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    total = x.shape[0] if total_tokens is None else total_tokens
+    C, K = w.shape
+    _check(_load().la_conv1d_silu_l2_prefill(
+        _ptr(conv_state_ptrs), _ptr(x), _ptr(w), _ptr(bias), _ptr(out), _ptr(cu_seqlens), B,
+        total, max_tokens if max_tokens is not None else total, C, K, l2_heads, head_dim,
+        float(eps), _row_stride(x), _row_stride(out), _dtype_code(x), _stream(stream)))
 
 
 def l2norm_heads(x, n_heads, head_dim, *, eps=1e-6, t=None, stream=None) -> None:

@@ -201,6 +201,34 @@ int la_conv1d_silu_prefill_varlen(const uint64_t *conv_state_ptrs, const void *x
     return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu launch");
 }
 
+int la_conv1d_silu_l2_prefill(const uint64_t *conv_state_ptrs, const void *x, const void *w,
+                              const void *bias, void *out, const int32_t *cu_seqlens, int B,
+                              int total_tokens, int max_tokens, int channels, int kernel,
+                              int l2_heads, int head_dim, float eps, int64_t x_stride,
+                              int64_t out_stride, int dtype, uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "conv1d of %d tokens does not fit max_tokens %d", total_tokens,
+                    max_tokens);
+    LA_TRY(conv_common(x, w, bias, out, channels, kernel, x_stride, out_stride, dtype));
+    if (B < 1) return fail(LA_ERR_ARG, "B must be >= 1 (got %d)", B);
+    if (!cu_seqlens && B != 1) return fail(LA_ERR_ARG, "cu_seqlens NULL requires B == 1");
+    if (kernel > 1 && !conv_state_ptrs) return fail(LA_ERR_ARG, "conv_state_ptrs is NULL");
+    if (head_dim != 64 && head_dim != 128)
+        return fail(LA_ERR_UNSUPPORTED, "head_dim %d: compiled for 64 and 128", head_dim);
+    if (l2_heads < 0 || (int64_t)l2_heads * head_dim > channels)
+        return fail(LA_ERR_ARG, "l2_heads * head_dim (%d x %d) exceeds channels (%d)", l2_heads,
+                    head_dim, channels);
+    if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
+    la::ConvArgs a{};
+    a.state_ptrs = conv_state_ptrs;
+    a.x = x; a.w = w; a.bias = bias; a.out = out;
+    a.cu = cu_seqlens; a.B = B; a.total = total_tokens; a.channels = channels; a.kernel = kernel;
+    a.x_stride = x_stride; a.out_stride = out_stride; a.dtype = dtype;
+    a.l2_heads = l2_heads; a.head_dim = head_dim; a.eps = eps;
+    a.status = status_ptr();
+    return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu_l2 launch");
+}
+
 int la_l2norm_heads(void *x, int t, int n_heads, int head_dim, int64_t row_stride, float eps,
                     int dtype, uint64_t stream) {
     if (t <= 0) return fail(LA_ERR_COUNT, "l2norm of %d tokens", t);

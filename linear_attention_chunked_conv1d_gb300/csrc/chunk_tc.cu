@@ -39,7 +39,8 @@ namespace {
 
 constexpr int TC_C = 64;         // chunk
 constexpr int TC_D = 128;        // dk = dv
-constexpr int TC_THREADS = 256;  // 8 warps: warp w owns TMEM lanes 32*(w%4).. and column half w/4
+constexpr int TC_THREADS = 512;  // 16 warps: warp w owns TMEM lanes 32*(w%4).. and column quarter w/4
+constexpr int NQ = TC_THREADS / 128;  // column parts per TMEM lane
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 // TMEM columns. D1 (K K^T | Q K^T) and D6 (U'^T) share columns: D1 is consumed before D6 is
@@ -57,13 +58,18 @@ constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t]: K^
 constexpr uint32_t SM_P = SM_KDT + 32768;        // tf32 SW128 [64 t][64 i]
 constexpr uint32_t SM_T = SM_P + 16384;          // tf32 SW128 [64 t][64 i]
 constexpr uint32_t SM_ID = SM_T + 16384;         // bf16 SW128 [64][64] identity
-constexpr uint32_t SM_AT = SM_ID + 8192;         // fp32 A^T split by row class: [64 i][4][20]
-constexpr uint32_t AT_I = 80, AT_P = 20;         // floats per i row / per row class
-constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_I * 4;
+constexpr uint32_t AT_LD = 68;                   // padded row of the fp32 A^T tile
+constexpr uint32_t SM_AT = SM_ID + 8192;         // fp32 A^T [64 i][68]; later the bf16 O tile
+constexpr uint32_t SL_LD = 36;                   // padded row of the 32x32 solver tiles
+constexpr uint32_t SM_T00 = SM_AT + 64 * AT_LD * 4;   // fp32 T00 [32][36]
+constexpr uint32_t SM_T11T = SM_T00 + 32 * SL_LD * 4; // fp32 T11^T [32][36]
+constexpr uint32_t SM_Y = SM_T11T + 32 * SL_LD * 4;   // fp32 A10 T00 [32][36]
+constexpr uint32_t O_LD = 136;                   // padded row (bf16) of the output staging tile
+constexpr uint32_t SM_SMALL = SM_Y + 32 * SL_LD * 4;
 // small region (floats)
 constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 256,
-                   SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704, SF_WARP = 832,
-                   SF_END = 840;
+                   SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704 /* [NQ][128] */,
+                   SF_WARP = 704 + 128 * NQ, SF_END = SF_WARP + 8;
 constexpr uint32_t SM_BYTES = SM_SMALL + SF_END * 4 + 64;  // + mbarriers, flags, tmem base
 constexpr size_t TC_SMEM = SM_BYTES + 1024;                // alignment slack
 constexpr float LOG2E = 1.4426950408889634f;
@@ -115,7 +121,7 @@ __device__ __forceinline__ void load_kq(const RecArgs &a, unsigned char *sm, int
     const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) + (int64_t)kh * TC_D;
     const uint32_t base = tc::smem_u32(sm + SM_KQ);
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < 2048 / TC_THREADS; ++m) {
         const int idx = tid + TC_THREADS * m;  // 0..2047
         const int which = idx >> 10, rem = idx & 1023;
         const int row = rem >> 4, ch = rem & 15;
@@ -131,7 +137,7 @@ __device__ __forceinline__ void load_v(const RecArgs &a, unsigned char *sm, int 
     const __nv_bfloat16 *vp = reinterpret_cast<const __nv_bfloat16 *>(a.v) + (int64_t)j * TC_D;
     const uint32_t base = tc::smem_u32(sm + SM_V);
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < 1024 / TC_THREADS; ++m) {
         const int idx = tid + TC_THREADS * m;  // 0..1023
         const int row = idx >> 4, ch = idx & 15;
         const bool valid = row < n;
@@ -155,7 +161,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
     float *sf = reinterpret_cast<float *>(sm + SM_SMALL);
-    float *at4 = reinterpret_cast<float *>(sm + SM_AT);
+    float *atp = reinterpret_cast<float *>(sm + SM_AT);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_SMALL + SF_END * 4);
     uint64_t *bar_b = bar_a + 1;
     volatile int *err = reinterpret_cast<volatile int *>(sm + SM_SMALL + SF_END * 4 + 16);
@@ -165,10 +171,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t lq = tc::tmem_lane_base(warp);  // this warp's TMEM lane quadrant
-    // TMEM row (= k-channel c when staging, = v-channel d in the state phases) and the half of
-    // the columns (or of the chunk's rows) this thread takes.
+    // TMEM row (= k-channel c when staging, = v-channel d in the state phases) and which of the
+    // NQ parts of the columns (or of the chunk's rows) this thread takes.
     const int row = tid & 127;
-    const int half = tid >> 7;
+    const int part = tid >> 7;
+    constexpr int C16 = TC_C / NQ;   // chunk rows / 64-column slices per part
+    constexpr int D32 = TC_D / NQ;   // 128-column slices per part
 
     if (tid == 0) {
         *err = 0;
@@ -191,6 +199,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = *tmem_sh;
+    const uint32_t sb = tc::smem_u32(sm);  // shared-window address of the tile area (uniform)
     uint32_t phase_a = 0, phase_b = 0;
 
     auto wait_bar = [&](uint64_t *bar, uint32_t &ph) {
@@ -207,7 +216,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
     const float scale = a.scale;
     const int Hv = a.Hv, group = a.Hv / a.Hk;
-    const int sj = 8 * warp + (lane >> 2), sp = lane & 3;  // solver: column j, rows 4m + p
 
     for (;;) {
         __syncthreads();  // everyone has read the previous unit index
@@ -228,15 +236,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         load_kq(a, sm, t0, min(TC_C, len), kh, tid);
         load_v(a, sm, t0, min(TC_C, len), j, tid);
         cp_async_commit();
-        // S[d][c] = H[c][d]: thread (d, half) loads columns c in [64*half, 64*half + 64)
+        // S[d][c] = H[c][d]: thread (d, part) loads columns c in [D32*part, D32*part + D32)
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < D32 / 16; ++g) {
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = hg[(int64_t)(64 * half + g * 16 + i) * TC_D + row];
-            tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + 64 * half + g * 16), v);
+            for (int i = 0; i < 16; ++i) v[i] = hg[(int64_t)(D32 * part + g * 16 + i) * TC_D + row];
+            tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + D32 * part + g * 16), v);
         }
         tc::tmem_wait_st();
+
+        // gate and beta of the chunk being computed are fetched one chunk ahead (threads < 64)
+        float pre_g = 0.f, pre_b = 0.f;
+        auto fetch_gates = [&](int tok, int nn) {
+            if (tid < TC_C) {
+                pre_b = tid < nn ? a.beta[(int64_t)(tok + tid) * Hv + j] : 0.f;
+                if (!KDA) pre_g = tid < nn ? a.g[(int64_t)(tok + tid) * Hv + j] : 0.f;
+            }
+        };
+        fetch_gates(t0, min(TC_C, len));
 
         for (int ch = 0; ch < nch; ++ch) {
             const int tok0 = t0 + ch * TC_C;
@@ -244,24 +262,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             const bool last = (ch + 1 == nch);
 
             // ---------------- gates
-            float gcr[KDA ? 32 : 1];  // KDA: gc[32*half + t][c], c = row
+            float gcr[KDA ? C16 : 1];  // KDA: gc[C16*part + t][c], c = row
             if (KDA) {
                 const float *gp = a.g + ((int64_t)tok0 * Hv + j) * TC_D + row;
                 float acc = 0.f;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int tt = 32 * half + t;
+                for (int t = 0; t < C16; ++t) {
+                    const int tt = C16 * part + t;
                     acc += tt < n ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
                     gcr[t] = acc;
                 }
-                if (half == 0) sf[SF_CARRY + row] = acc;
+                sf[SF_CARRY + part * 128 + row] = acc;
                 if (tid == 0) *slow_sh = 0;
             }
             if (tid < TC_C) {
                 const int t = tid;
-                sf[SF_BETA + t] = t < n ? a.beta[(int64_t)(tok0 + t) * Hv + j] : 0.f;
+                sf[SF_BETA + t] = pre_b;
                 if (!KDA) {
-                    float x = t < n ? a.g[(int64_t)(tok0 + t) * Hv + j] : 0.f;
+                    float x = pre_g;
 #pragma unroll
                     for (int off = 1; off < 32; off <<= 1) {
                         const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -275,15 +293,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             tc::fence_async_smem();
             if (!sync_ok(err)) break;
             if (KDA) {
-                if (half == 1) {
-                    const float carry = sf[SF_CARRY + row];
+                float carry = 0.f;
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) gcr[t] += carry;
-                    sf[SF_GL + row] = gcr[31];
-                    sf[SF_EL + row] = __expf(gcr[31]);
-                } else {
-                    sf[SF_GM + row] = gcr[31];
+                for (int pp = 0; pp < NQ - 1; ++pp)
+                    if (pp < part) carry += sf[SF_CARRY + pp * 128 + row];
+#pragma unroll
+                for (int t = 0; t < C16; ++t) gcr[t] += carry;
+                if (part == NQ - 1) {
+                    sf[SF_GL + row] = gcr[C16 - 1];
+                    sf[SF_EL + row] = __expf(gcr[C16 - 1]);
                 }
+                if (part == NQ / 2 - 1) sf[SF_GM + row] = gcr[C16 - 1];
             } else if (tid < TC_C) {
                 const float gct = sf[SF_GC + tid] + (tid >= 32 ? sf[SF_WARP] : 0.f);
                 sf[SF_GC + tid] = gct;
@@ -315,10 +335,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 const int c = row;
                 const float gm = sf[SF_GM + c];
                 const float gLc = sf[SF_GL + c];
-                if (half == 0 ? (-gm > 80.f) : (gm - gLc > 80.f)) *slow_sh = 1;
+                if (part == NQ / 2 - 1 && -gm > 80.f) *slow_sh = 1;
+                if (part == NQ - 1 && gm - gLc > 80.f) *slow_sh = 1;
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int tt = 32 * half + t;
+                for (int t = 0; t < C16; ++t) {
+                    const int tt = C16 * part + t;
                     const float kv = ld_bf16(sm, w_kq.at(tt));
                     const float qv = ld_bf16(sm, w_kq.at(64 + tt));
                     const float f1 = __expf(gcr[t] - gm), f2 = __expf(gm - gcr[t]);
@@ -332,30 +353,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
             tc::fence_before_sync();
             __syncthreads();
-            if (!slow && tid == 0) {
+            if (!slow && warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
                 if (KDA) {
                     constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_TF32);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 16; ++kk) {
                         const uint32_t off = (kk & 3u) * 32u;
-                        const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sm + SM_KQG) + (kk >> 2) * 16384u + off);
-                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_KDT) + (kk >> 2) * 8192u + off);
+                        const uint64_t ad = tc::sdesc_sw128((sb + SM_KQG) + (kk >> 2) * 16384u + off);
+                        const uint64_t bd = tc::sdesc_sw128((sb + SM_KDT) + (kk >> 2) * 8192u + off);
                         tc::mma_tf32_ss(tm + COL_D1, ad, bd, id, kk > 0);
                     }
                 } else {
                     constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_BF16);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 8; ++kk) {
-                        const uint32_t addr = tc::smem_u32(sm + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u;
+                        const uint32_t addr = (sb + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u;
                         tc::mma_bf16_ss(tm + COL_D1, tc::sdesc_sw128(addr), tc::sdesc_sw128(addr), id, kk > 0);
                     }
                     // K^T[c][t] = sum_i K[i][c] I[t][i]: A = K tile read MN-major
                     constexpr uint32_t idt = tc::idesc(128, 64, tc::FMT_BF16, true, false);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = tc::sdesc_sw128_mn(tc::smem_u32(sm + SM_KQ) + kk * 2048u, 128u * 128u, 1024u);
-                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_ID) + kk * 32u);
+                        const uint64_t ad = tc::sdesc_sw128_mn((sb + SM_KQ) + kk * 2048u, 128u * 128u, 1024u);
+                        const uint64_t bd = tc::sdesc_sw128((sb + SM_ID) + kk * 32u);
                         tc::mma_bf16_ss(tm + COL_D4, ad, bd, idt, kk > 0);
                     }
                 }
@@ -364,11 +385,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
             // ---- state-MMA operands. GDN: exact tf32 copy of [K;Q] (the gate factors are
             //      applied to the MMA results instead). KDA: [K e^gc ; Q e^gc] and
-            //      (K e^{gc_L - gc})^T, thread per (channel, row half).
+            //      (K e^{gc_L - gc})^T, thread per (channel, row part).
             auto stage_state_operands = [&]() {
                 if (!KDA) {
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
+                    for (int m = 0; m < 2048 / TC_THREADS; ++m) {
                         const int idx = tid + TC_THREADS * m;  // 0..2047 chunks of 8 elements
                         const int r = idx >> 4, cj = idx & 15;
                         const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
@@ -389,8 +410,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     const float gLc = sf[SF_GL + c];
                     float kd[4];
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        const int tt = 32 * half + t;
+                    for (int t = 0; t < C16; ++t) {
+                        const int tt = C16 * part + t;
                         const bool valid = tt < n;
                         const float kv = ld_bf16(sm, w_kq.at(tt));
                         const float qv = ld_bf16(sm, w_kq.at(64 + tt));
@@ -410,19 +431,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             auto issue_mma2 = [&]() {
                 tc::fence_before_sync();
                 __syncthreads();
-                if (tid == 0) {
+                if (warp == 0 && tc::elect_one()) {
                     tc::fence_after_sync();
                     constexpr uint32_t id = tc::idesc(128, 128, tc::FMT_TF32);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 16; ++kk) {
-                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_KQG) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                        const uint64_t bd = tc::sdesc_sw128((sb + SM_KQG) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
                         tc::mma_tf32_ts(tm + COL_D2, tm + COL_S + kk * 8, bd, id, kk > 0);
                     }
                     constexpr uint32_t idv = tc::idesc(128, 64, tc::FMT_BF16, true, false);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = tc::sdesc_sw128_mn(tc::smem_u32(sm + SM_V) + kk * 2048u, 64u * 128u, 1024u);
-                        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_ID) + kk * 32u);
+                        const uint64_t ad = tc::sdesc_sw128_mn((sb + SM_V) + kk * 2048u, 64u * 128u, 1024u);
+                        const uint64_t bd = tc::sdesc_sw128((sb + SM_ID) + kk * 32u);
                         tc::mma_bf16_ss(tm + COL_RUD, ad, bd, idv, kk > 0);
                     }
                     tc::mma_commit(bar_b);
@@ -440,9 +461,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             } else if (KDA) {
                 float *gct = reinterpret_cast<float *>(sm + SM_KQG);  // [64][128] fp32
 #pragma unroll
-                for (int t = 0; t < 32; ++t) gct[(32 * half + t) * TC_D + row] = gcr[t];
+                for (int t = 0; t < C16; ++t) gct[(C16 * part + t) * TC_D + row] = gcr[t];
                 __syncthreads();
-                if (half == 0) {  // warps 0-3: thread = D1 row
+                if (part == 0) {  // warps 0-3: thread = D1 row
                     const int r = row & 63;
                     const bool isq = row >= 64;
                     for (int g = 0; g < 4; ++g) {
@@ -469,54 +490,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
             if (!sync_ok(err)) break;
 
-            // ---------------- A^T (fp32, split by row class) and P (tf32) from D1; GDN: K^T tile
+            // ---------------- A^T (fp32) and P (tf32) from D1; GDN: K^T tile
             {
                 const int r = row & 63;
                 const bool isq = row >= 64;
                 const float gct2 = KDA ? 0.f : sf[SF_GC2 + r];
                 const float bt = sf[SF_BETA + r];
                 const bool rv = r < n;
+                const int i0 = C16 * part;
+                float v[16], kt[16];
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D1 + i0), v);
+                if (!KDA) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + i0), kt);
+                tc::tmem_wait_ld();
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const int i0 = 32 * half + 16 * g;
-                    float v[16];
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D1 + i0), v);
-                    tc::tmem_wait_ld();
+                for (int ii = 0; ii < 16; ++ii) {
+                    const int i = i0 + ii;
+                    const float dec = KDA ? 1.f : tc::ex2(fminf(gct2 - sf[SF_GC2 + i], 0.f));
+                    v[ii] = isq ? ((rv && i <= r) ? dec * v[ii] : 0.f)
+                                : ((rv && i < r) ? bt * dec * v[ii] : 0.f);
+                }
+                if (isq) {
 #pragma unroll
-                    for (int ii = 0; ii < 16; ++ii) {
-                        const int i = i0 + ii;
-                        const float dec = KDA ? 1.f : exp2f(gct2 - sf[SF_GC2 + i]);
-                        v[ii] = isq ? ((rv && i <= r) ? dec * v[ii] : 0.f)
-                                    : ((rv && i < r) ? bt * dec * v[ii] : 0.f);
-                    }
-                    if (isq) {
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        *reinterpret_cast<float4 *>(sm + SM_P + tc::sw128_offset(r, i0 + q4 * 4, 64, 4)) =
+                            make_float4(tc::to_tf32(v[q4 * 4]), tc::to_tf32(v[q4 * 4 + 1]),
+                                        tc::to_tf32(v[q4 * 4 + 2]), tc::to_tf32(v[q4 * 4 + 3]));
+                } else {
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<float4 *>(sm + SM_P + tc::sw128_offset(r, i0 + q4 * 4, 64, 4)) =
-                                make_float4(tc::to_tf32(v[q4 * 4]), tc::to_tf32(v[q4 * 4 + 1]),
-                                            tc::to_tf32(v[q4 * 4 + 2]), tc::to_tf32(v[q4 * 4 + 3]));
-                    } else {
-#pragma unroll
-                        for (int ii = 0; ii < 16; ++ii)
-                            at4[(i0 + ii) * AT_I + (r & 3) * AT_P + (r >> 2)] = v[ii];
-                    }
+                    for (int ii = 0; ii < 16; ++ii) atp[(i0 + ii) * AT_LD + r] = v[ii];
                 }
                 if (!KDA) {
                     // K^T[c][t] (exact in tf32) -> the [c][t] tile; columns t >= n zeroed
                     const int c = row;
 #pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        const int t0c = 32 * half + 16 * g;
-                        float v[16];
-                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), v);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int t = t0c + q4 * 4;
-                            *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, t, 128, 4)) =
-                                make_float4(t + 0 < n ? v[q4 * 4 + 0] : 0.f, t + 1 < n ? v[q4 * 4 + 1] : 0.f,
-                                            t + 2 < n ? v[q4 * 4 + 2] : 0.f, t + 3 < n ? v[q4 * 4 + 3] : 0.f);
-                        }
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int t = i0 + q4 * 4;
+                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, t, 128, 4)) =
+                            make_float4(t + 0 < n ? kt[q4 * 4 + 0] : 0.f, t + 1 < n ? kt[q4 * 4 + 1] : 0.f,
+                                        t + 2 < n ? kt[q4 * 4 + 2] : 0.f, t + 3 < n ? kt[q4 * 4 + 3] : 0.f);
                     }
                 }
             }
@@ -528,32 +539,77 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 issue_mma2();
             }
 
-            // ---------------- T = (I + A)^{-1}: 4 threads per column j, rows 4m + p
+            // ---------------- T = (I + A)^{-1} in 32x32 blocks, fp32 on CUDA cores:
+            //   T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} by forward substitution (8 threads per
+            //   column, rows 8m + p), then T10 = -T11 (A10 T00) as two 32x32x32 products.
             {
-                float x[16];
+                float *t00 = reinterpret_cast<float *>(sm + SM_T00);
+                float *t11t = reinterpret_cast<float *>(sm + SM_T11T);
+                float *ys = reinterpret_cast<float *>(sm + SM_Y);
+                {
+                    const int b = warp >> 3, o = 32 * b;
+                    const int jj = 4 * (warp & 7) + (lane >> 3), p = lane & 7;
+                    float x[4];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) x[m] = (4 * m + sp == sj) ? 1.f : 0.f;
-                const float *atp = at4 + sp * AT_P;
+                    for (int m = 0; m < 4; ++m) x[m] = (8 * m + p == jj) ? 1.f : 0.f;
+                    const float *ab = atp + o * AT_LD + o + p;  // ab[i*AT_LD + 8m] = A[o+8m+p][o+i]
 #pragma unroll
-                for (int i = 0; i < TC_C - 1; ++i) {
-                    const int m0 = i >> 2;
-                    const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~3) | (i & 3));
-                    {
-                        const float nx = fmaf(-atp[i * AT_I + m0], xi, x[m0]);
-                        x[m0] = (sp > (i & 3)) ? nx : x[m0];
+                    for (int i = 0; i < 31; ++i) {
+                        const int m0 = i >> 3;
+                        const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~7) | (i & 7));
+                        {
+                            const float nx = fmaf(-ab[i * AT_LD + 8 * m0], xi, x[m0]);
+                            x[m0] = (p > (i & 7)) ? nx : x[m0];
+                        }
+#pragma unroll
+                        for (int m = m0 + 1; m < 4; ++m) x[m] = fmaf(-ab[i * AT_LD + 8 * m], xi, x[m]);
                     }
 #pragma unroll
-                    for (int m = m0 + 1; m < 16; ++m) x[m] = fmaf(-atp[i * AT_I + m], xi, x[m]);
+                    for (int m = 0; m < 4; ++m) {
+                        const int t = 8 * m + p;
+                        st_tf32(sm, SM_T + tc::sw128_offset(o + t, o + jj, 64, 4), x[m]);
+                        if (b == 0) {
+                            st_tf32(sm, SM_T + tc::sw128_offset(t, 32 + jj, 64, 4), 0.f);  // T01 = 0
+                            t00[t * SL_LD + jj] = x[m];
+                        } else {
+                            t11t[jj * SL_LD + t] = x[m];
+                        }
+                    }
                 }
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    st_tf32(sm, SM_T + tc::sw128_offset(4 * m + sp, sj, 64, 4), x[m]);
+                __syncthreads();
+                const int jc = lane, tq = warp;  // output rows 2tq, 2tq+1; column jc
+                {   // Y = A10 T00, A10[t][i] = A[32 + t][i]
+                    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 a2 = *reinterpret_cast<const float2 *>(atp + i * AT_LD + 32 + 2 * tq);
+                        const float tv = t00[i * SL_LD + jc];
+                        acc0 = fmaf(a2.x, tv, acc0);
+                        acc1 = fmaf(a2.y, tv, acc1);
+                    }
+                    ys[(2 * tq) * SL_LD + jc] = acc0;
+                    ys[(2 * tq + 1) * SL_LD + jc] = acc1;
+                }
+                __syncthreads();
+                {   // T10 = -T11 Y
+                    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 t2 = *reinterpret_cast<const float2 *>(t11t + i * SL_LD + 2 * tq);
+                        const float yv = ys[i * SL_LD + jc];
+                        acc0 = fmaf(t2.x, yv, acc0);
+                        acc1 = fmaf(t2.y, yv, acc1);
+                    }
+                    st_tf32(sm, SM_T + tc::sw128_offset(32 + 2 * tq, jc, 64, 4), -acc0);
+                    st_tf32(sm, SM_T + tc::sw128_offset(32 + 2 * tq + 1, jc, 64, 4), -acc1);
+                }
             }
             tc::fence_async_smem();
             __syncthreads();
-            if (!last) {  // K|Q tile is free: next chunk's K, Q in flight
+            if (!last) {  // K|Q tile is free: next chunk's K, Q (and gates) in flight
                 load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
+                fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
             }
 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})
@@ -564,44 +620,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 cp_async_commit();
             }
             {
+                const int t0c = C16 * part, c0 = D32 * part;
+                float v[16], vt[16], sv[D32];
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + t0c), v);
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RUD + t0c), vt);
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const int t0c = 32 * half + 16 * g;
-                    float v[16], vt[16];
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + t0c), v);
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RUD + t0c), vt);
-                    tc::tmem_wait_ld();
+                for (int g = 0; g < D32 / 16; ++g)
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
+                tc::tmem_wait_ld();
 #pragma unroll
-                    for (int ii = 0; ii < 16; ++ii) {
-                        const int t = t0c + ii;
-                        const float kh_t = KDA ? v[ii] : sf[SF_EG + t] * v[ii];
-                        v[ii] = t < n ? tc::to_tf32(sf[SF_BETA + t] * (vt[ii] - kh_t)) : 0.f;
-                    }
-                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                for (int ii = 0; ii < 16; ++ii) {
+                    const int t = t0c + ii;
+                    const float kh_t = KDA ? v[ii] : sf[SF_EG + t] * v[ii];
+                    v[ii] = t < n ? tc::to_tf32(sf[SF_BETA + t] * (vt[ii] - kh_t)) : 0.f;
                 }
                 const float egL = KDA ? 0.f : sf[SF_EG + TC_C - 1];
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int c0 = 64 * half + 16 * g;
-                    float v[16];
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + c0), v);
-                    tc::tmem_wait_ld();
+                for (int ii = 0; ii < D32; ++ii) sv[ii] *= KDA ? sf[SF_EL + c0 + ii] : egL;
+                tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
 #pragma unroll
-                    for (int ii = 0; ii < 16; ++ii) v[ii] *= KDA ? sf[SF_EL + c0 + ii] : egL;
-                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0), v);
-                }
+                for (int g = 0; g < D32 / 16; ++g)
+                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
                 tc::tmem_wait_st();
             }
             tc::fence_before_sync();
             __syncthreads();
 
             // ---------------- U'^T = R^T T^T
-            if (tid == 0) {
+            if (warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
                 constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_TF32);
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sm + SM_T) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
+                    const uint64_t bd = tc::sdesc_sw128((sb + SM_T) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
                     tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8, bd, id, kk > 0);
                 }
                 tc::mma_commit(bar_b);
@@ -610,13 +661,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             if (!sync_ok(err)) break;
 
             // ------ U'^T -> TMEM (tf32); GDN also U'^T diag(e^{gc_L - gc}) for the state update
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int t0c = 32 * half + 16 * g;
-                float v[16];
+            {
+                const int t0c = C16 * part;
+                float v[16], w[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);
                 tc::tmem_wait_ld();
-                float w[16];
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
                     w[ii] = KDA ? 0.f : tc::to_tf32(v[ii] * sf[SF_EGL + t0c + ii]);
@@ -630,19 +679,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             __syncthreads();
 
             // ---------------- D4 = U'^T P^T ; S += U'd^T K (GDN) or U'^T Kdec (KDA)
-            if (tid == 0) {
+            if (warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
                 constexpr uint32_t id64 = tc::idesc(128, 64, tc::FMT_TF32);
                 constexpr uint32_t id128 = tc::idesc(128, 128, tc::FMT_TF32);
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
-                    const uint64_t bp = tc::sdesc_sw128(tc::smem_u32(sm + SM_P) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
+                    const uint64_t bp = tc::sdesc_sw128((sb + SM_P) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
                     tc::mma_tf32_ts(tm + COL_D4, tm + COL_RU + kk * 8, bp, id64, kk > 0);
                 }
                 const uint32_t a5 = KDA ? COL_RU : COL_RUD;
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
-                    const uint64_t bk = tc::sdesc_sw128(tc::smem_u32(sm + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                    const uint64_t bk = tc::sdesc_sw128((sb + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
                     tc::mma_tf32_ts(tm + COL_S, tm + a5 + kk * 8, bk, id128, 1);
                 }
                 tc::mma_commit(bar_b);
@@ -650,10 +699,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
 
-            // ---------------- o = scale (e^gc (Q H) + P U'), rows < n
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const int t0c = 32 * half + 16 * g;
+            // ---------------- o = scale (e^gc (Q H) + P U'): staged as bf16 [t][d] in shared
+            //                  memory, then written with 16-byte stores, rows < n
+            {
+                __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + SM_AT);
+                const int t0c = C16 * part;
                 float vq[16], vp[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
@@ -662,7 +712,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 for (int ii = 0; ii < 16; ++ii) {
                     const int t = t0c + ii;
                     const float o = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
-                    if (t < n) og[(int64_t)(tok0 + t) * Hv * TC_D + row] = __float2bfloat16_rn(scale * o);
+                    os[t * O_LD + row] = __float2bfloat16_rn(scale * o);
+                }
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < 1024 / TC_THREADS; ++m) {
+                    const int idx = tid + TC_THREADS * m;  // 0..1023
+                    const int t = idx >> 4, cj = idx & 15;
+                    if (t < n)
+                        *reinterpret_cast<uint4 *>(og + (int64_t)(tok0 + t) * Hv * TC_D + cj * 8) =
+                            *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
                 }
             }
             tc::fence_before_sync();
@@ -673,12 +732,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
         // state back: H[c][d] = S[d][c]
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < D32 / 16; ++g) {
             float v[16];
-            tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + 64 * half + g * 16), v);
+            tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + D32 * part + g * 16), v);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) hg[(int64_t)(64 * half + g * 16 + i) * TC_D + row] = v[i];
+            for (int i = 0; i < 16; ++i) hg[(int64_t)(D32 * part + g * 16 + i) * TC_D + row] = v[i];
         }
         tc::fence_before_sync();
         __syncthreads();

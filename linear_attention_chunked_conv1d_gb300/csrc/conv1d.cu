@@ -1,4 +1,5 @@
-// Causal depthwise conv1d + SiLU with a carried conv state, single stream or varlen.
+// Causal depthwise conv1d + SiLU with a carried conv state, single stream or varlen, optionally
+// fused with the per-head L2 norm of the q|k channels.
 //
 // Page: "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill, conv_prefill launch
 // (conv + SiLU only; the fourth pointer slot, read here as an optional bias, is NULL there);
@@ -26,24 +27,33 @@ __device__ __forceinline__ int conv_run_base(const int32_t *cu, int s) {
     return cu[s] / CONV_ROWS + s;
 }
 
-template <typename T, int K>
-__global__ void __launch_bounds__(CONV_THREADS)
+// HD > 0: also L2-normalise, per (token, head), the first n_l2 channels (whole heads of HD
+// channels). The conv output is rounded to T first, exactly as the separate l2 launch would
+// read it back, and the sum of squares is reduced in the same order as that launch, so the
+// fused and the two-launch paths give identical bits.
+// SiLU(y) = y sigmoid(y) = y / (1 + e^-y), with the fast exponential and reciprocal.
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
+
+template <typename T, int K, int HD>
+__global__ void __launch_bounds__(CONV_THREADS, 4)
 conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                    const T *__restrict__ x, const T *__restrict__ w,
                    const T *__restrict__ bias, T *__restrict__ out,
                    const int32_t *__restrict__ cu, int B, int total, int C, int64_t xs,
-                   int64_t os, int *status) {
+                   int64_t os, int n_l2, float eps, int *status) {
     using V = Vec16<T>;
     constexpr int N = V::N;
+    constexpr int LPH = HD > 0 ? HD / N : 1;  // lanes per head
     const int cv = blockIdx.y * CONV_THREADS + threadIdx.x;
     const int c0 = cv * N;
-    if (c0 >= C) return;
+    const bool active = c0 < C;  // inactive lanes still take part in the head reductions
+    const bool do_l2 = HD > 0 && c0 < n_l2;
 
     // Which stream and which run of it this block covers.
     int s = 0, sb = 0, se = total, run = blockIdx.x;
     if (cu) {
         if (cu[0] != 0 || cu[B] != total) {
-            raise_status(status, LA_DEV_BAD_SEQLENS);
+            if (threadIdx.x == 0) raise_status(status, LA_DEV_BAD_SEQLENS);
             return;
         }
         const int y = blockIdx.x;
@@ -56,32 +66,33 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
         sb = cu[s];
         se = cu[s + 1];
         if (se < sb || se > total) {
-            raise_status(status, LA_DEV_BAD_SEQLENS);
+            if (threadIdx.x == 0) raise_status(status, LA_DEV_BAD_SEQLENS);
             return;
         }
         run = y - conv_run_base(cu, s);
     }
     const int r0 = sb + run * CONV_ROWS;
-    if (run < 0 || r0 >= se) return;  // slot past this stream's runs
+    if (run < 0 || r0 >= se) return;  // slot past this stream's runs (uniform per block)
     const int r1 = min(r0 + CONV_ROWS, se);
 
     float wr[N][K];
-#pragma unroll
-    for (int e = 0; e < N; ++e)
-#pragma unroll
-        for (int j = 0; j < K; ++j) wr[e][j] = to_f(w[(int64_t)(c0 + e) * K + j]);
     float br[N];
-    if (bias) {
-        V::load(bias + c0, br);
-    } else {
 #pragma unroll
-        for (int e = 0; e < N; ++e) br[e] = 0.f;
+    for (int e = 0; e < N; ++e) {
+        br[e] = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) wr[e][j] = active ? to_f(w[(int64_t)(c0 + e) * K + j]) : 0.f;
     }
+    if (bias && active) V::load(bias + c0, br);
 
     // win[m] = row (tau - (K-1) + m) of xh = [state ; x] for the current tau.
     float win[K > 1 ? K - 1 : 1][N];
+#pragma unroll
+    for (int m = 0; m < (K > 1 ? K - 1 : 1); ++m)
+#pragma unroll
+        for (int e = 0; e < N; ++e) win[m][e] = 0.f;
     if constexpr (K > 1) {
-        if (run == 0) {
+        if (active && run == 0) {
             // Only reader of this stream's state: read it, fill the window, then advance it.
             T *st = state_ptrs ? reinterpret_cast<T *>(state_ptrs[s]) : single_state;
             float old[K - 1][N];
@@ -108,38 +119,68 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                 }
                 V::store(st + (int64_t)m * C + c0, nv);
             }
-        } else {
+        } else if (active) {
 #pragma unroll
             for (int m = 0; m < K - 1; ++m)
                 V::load(x + (int64_t)(r0 - (K - 1) + m) * xs + c0, win[m]);
         }
     }
 
-    for (int tau = r0; tau < r1; ++tau) {
-        float cur[N];
-        V::load(x + (int64_t)tau * xs + c0, cur);
-        float y[N];
+    // rows in groups of 4: the 4 loads are issued before any of them is used
+    constexpr int G = 4;
+    for (int g0 = r0; g0 < r1; g0 += G) {
+        float cur[G][N];
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-            float acc = br[e];
+        for (int q = 0; q < G; ++q) {
+            if (active && g0 + q < r1) {
+                V::load(x + (int64_t)(g0 + q) * xs + c0, cur[q]);
+            } else {
 #pragma unroll
-            for (int m = 0; m < K - 1; ++m) acc = fmaf(wr[e][m], win[m][e], acc);
-            acc = fmaf(wr[e][K - 1], cur[e], acc);
-            y[e] = acc / (1.f + expf(-acc));
+                for (int e = 0; e < N; ++e) cur[q][e] = 0.f;
+            }
         }
-        V::store(out + (int64_t)tau * os + c0, y);
-        if constexpr (K > 1) {
 #pragma unroll
-            for (int m = 0; m < K - 2; ++m)
+        for (int q = 0; q < G; ++q) {
+            float y[N];
 #pragma unroll
-                for (int e = 0; e < N; ++e) win[m][e] = win[m + 1][e];
+            for (int e = 0; e < N; ++e) {
+                float acc = br[e];
 #pragma unroll
-            for (int e = 0; e < N; ++e) win[K - 2][e] = cur[e];
+                for (int m = 0; m < K - 1; ++m) acc = fmaf(wr[e][m], win[m][e], acc);
+                acc = fmaf(wr[e][K - 1], cur[q][e], acc);
+                y[e] = silu(acc);
+            }
+            if constexpr (HD > 0) {
+                // round to the stored type, then the same reduction as the l2 launch
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < N; ++e) {
+                    y[e] = to_f(from_f<T>(y[e]));
+                    ss = fmaf(y[e], y[e], ss);
+                }
+#pragma unroll
+                for (int off = LPH / 2; off > 0; off >>= 1)
+                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (do_l2) {
+                    const float inv = 1.f / sqrtf(ss + eps);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) y[e] *= inv;
+                }
+            }
+            if (active && g0 + q < r1) V::store(out + (int64_t)(g0 + q) * os + c0, y);
+            if constexpr (K > 1) {
+#pragma unroll
+                for (int m = 0; m < K - 2; ++m)
+#pragma unroll
+                    for (int e = 0; e < N; ++e) win[m][e] = win[m + 1][e];
+#pragma unroll
+                for (int e = 0; e < N; ++e) win[K - 2][e] = cur[q][e];
+            }
         }
     }
 }
 
-template <typename T, int K>
+template <typename T, int K, int HD>
 static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
     constexpr int N = Vec16<T>::N;
     int nvec = a.channels / N;
@@ -147,25 +188,32 @@ static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
     // stream's runs (stream s starts at slot floor(cu[s]/ROWS) + s).
     int slots = a.cu ? a.total / CONV_ROWS + a.B : (a.total + CONV_ROWS - 1) / CONV_ROWS;
     dim3 grid(slots, (nvec + CONV_THREADS - 1) / CONV_THREADS);
-    conv1d_silu_kernel<T, K><<<grid, CONV_THREADS, 0, st>>>(
+    conv1d_silu_kernel<T, K, HD><<<grid, CONV_THREADS, 0, st>>>(
         a.state_ptrs, (T *)a.single_state, (const T *)a.x, (const T *)a.w, (const T *)a.bias,
-        (T *)a.out, a.cu, a.B, a.total, a.channels, a.x_stride, a.out_stride, a.status);
+        (T *)a.out, a.cu, a.B, a.total, a.channels, a.x_stride, a.out_stride,
+        a.l2_heads * a.head_dim, a.eps, a.status);
     return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, int HD>
 static cudaError_t launch_conv_k(const ConvArgs &a, cudaStream_t st) {
     switch (a.kernel) {
-        case 1: return launch_conv_t<T, 1>(a, st);
-        case 2: return launch_conv_t<T, 2>(a, st);
-        case 3: return launch_conv_t<T, 3>(a, st);
-        case 4: return launch_conv_t<T, 4>(a, st);
+        case 1: return launch_conv_t<T, 1, HD>(a, st);
+        case 2: return launch_conv_t<T, 2, HD>(a, st);
+        case 3: return launch_conv_t<T, 3, HD>(a, st);
+        case 4: return launch_conv_t<T, 4, HD>(a, st);
     }
     return cudaErrorInvalidValue;
 }
 
+template <typename T>
+static cudaError_t launch_conv_h(const ConvArgs &a, cudaStream_t st) {
+    if (a.l2_heads <= 0) return launch_conv_k<T, 0>(a, st);
+    return a.head_dim == 64 ? launch_conv_k<T, 64>(a, st) : launch_conv_k<T, 128>(a, st);
+}
+
 cudaError_t launch_conv1d_silu(const ConvArgs &a, cudaStream_t st) {
-    return a.dtype == LA_BF16 ? launch_conv_k<__nv_bfloat16>(a, st) : launch_conv_k<float>(a, st);
+    return a.dtype == LA_BF16 ? launch_conv_h<__nv_bfloat16>(a, st) : launch_conv_h<float>(a, st);
 }
 
 }  // namespace la

@@ -15,6 +15,8 @@ struct ConvArgs {
     int B, total, channels, kernel;
     int64_t x_stride, out_stride;
     int dtype;
+    int l2_heads, head_dim;  // l2_heads > 0: fused L2 over the first l2_heads * head_dim channels
+    float eps;
     int *status;
 };
 cudaError_t launch_conv1d_silu(const ConvArgs &a, cudaStream_t st);

@@ -208,6 +208,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// 2^x on the special-function unit (ex2.approx.ftz: relative error below 2^-22; x <= 0 in
+// every use here, so no overflow path is needed).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One lane of a converged warp (elect.sync): MMAs are issued by the elected lane of a fully
+// converged warp so that their descriptor operands stay warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Round-to-nearest conversion of fp32 to tf32 (kept in a 32-bit container).
 __device__ __forceinline__ float to_tf32(float x) {
     uint32_t r;

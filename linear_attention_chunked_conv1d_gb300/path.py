@@ -16,7 +16,8 @@ import math
 
 import torch
 
-from . import (conv1d_silu_prefill, conv1d_silu_prefill_varlen, gdn_prefill_batched,
+from . import (conv1d_silu_l2_prefill, conv1d_silu_prefill, conv1d_silu_prefill_varlen,
+               gdn_prefill_batched,
                gdn_prefill_varlen, kda_prefill, l2norm_heads, pointer_array,
                prefill_workspace_bytes)
 
@@ -52,6 +53,14 @@ class PrefillPass:
         self.scale = 1.0 / math.sqrt(wl.d)
 
     def front_end(self, stream=None):
+        """conv1d + SiLU and the q|k L2 norm in one fused launch (bitwise equal to the two)."""
+        wl, inp = self.wl, self.inp
+        conv1d_silu_l2_prefill(self.conv_state_ptrs, inp["x"], inp["conv_w"], self.conv_out,
+                               None if wl.B == 1 else inp["cu_seqlens"], l2_heads=2 * wl.Hk,
+                               head_dim=wl.d, eps=self.eps, stream=stream)
+
+    def front_end_unfused(self, stream=None):
+        """The pages' two launches: conv_prefill, then l2 in place over q|k."""
         wl, inp = self.wl, self.inp
         if wl.B == 1:
             conv1d_silu_prefill(inp["conv_state"][0], inp["x"], inp["conv_w"], self.conv_out,

@@ -308,3 +308,42 @@ def test_workspace_too_small_is_refused(cuda):
         la.gdn_prefill_batched(la.pointer_array([h[0]]), q, k, v, inp["g"].to(cuda),
                                inp["beta"].to(cuda), out, B=1, T=64, Hk=1, Hv=1, dk=128, dv=128)
     assert ei.value.code == la.LA_ERR_ARG
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("hd", [64, 128])
+@pytest.mark.parametrize("lengths", [[150], [1, 0, 70, 3, 129, 64]])
+def test_fused_conv_l2_equals_two_launches_and_oracle(cuda, dtype, hd, lengths):
+    g = gen(hd + len(lengths))
+    Hk, Hv, K = 2, 3, 4
+    C = 2 * Hk * hd + Hv * hd
+    T, B = sum(lengths), len(lengths)
+    x = torch.randn(T, C, generator=g).to(DT[dtype])
+    w = (torch.randn(C, K, generator=g) * 0.25).to(DT[dtype])
+    st = torch.randn(B, K - 1, C, generator=g).to(DT[dtype])
+    cu = torch.tensor([0] + list(np.cumsum(lengths)), dtype=torch.int32)
+    xd, wd, cud = x.to(cuda), w.to(cuda), cu.to(cuda)
+    st1, st2 = st.clone().to(cuda), st.clone().to(cuda)
+    o1 = torch.empty(T, C, dtype=DT[dtype], device=cuda)
+    o2 = torch.full((T, C), 9.0, dtype=DT[dtype], device=cuda)
+    p1 = la.pointer_array([st1[s] for s in range(B)])
+    p2 = la.pointer_array([st2[s] for s in range(B)])
+    if B == 1:
+        la.conv1d_silu_prefill(st1[0], xd, wd, o1)
+    else:
+        la.conv1d_silu_prefill_varlen(p1, xd, wd, o1, cud)
+    la.l2norm_heads(o1, 2 * Hk, hd, eps=1e-6)
+    la.conv1d_silu_l2_prefill(p2, xd, wd, o2, None if B == 1 else cud, l2_heads=2 * Hk,
+                              head_dim=hd, eps=1e-6)
+    torch.cuda.synchronize()
+    assert la.device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(st1, st2)
+    q, k, v, ref_st = oracle.front_end(f64(x), f64(w), f64(st), cu.numpy(), Hk=Hk, Hv=Hv,
+                                       dk=hd, dv=hd, eps=1e-6, act_dtype=dtype)
+    ref = np.concatenate([q.reshape(T, -1), k.reshape(T, -1), v.reshape(T, -1)], axis=1)
+    got = o2.cpu()
+    if dtype == "f32":
+        assert max_abs(f64(got), ref) <= 1e-5
+    else:
+        assert bf16_ulp_diff(got, ref) <= 1
+    np.testing.assert_array_equal(f64(st2.cpu()), ref_st)
