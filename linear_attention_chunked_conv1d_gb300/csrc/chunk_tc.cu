@@ -43,9 +43,10 @@ constexpr int TC_THREADS = 512;  // 16 warps: warp w owns TMEM lanes 32*(w%4).. 
 constexpr int NQ = TC_THREADS / 128;  // column parts per TMEM lane
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
-// TMEM columns. D1 (K K^T | Q K^T) and D6 (U'^T) share columns: D1 is consumed before D6 is
-// produced. V^T (identity MMA) lands in the U'd^T columns before they are reused; K^T (identity
-// MMA, GDN) lands in the P U' accumulator columns before MMA4 overwrites them.
+// TMEM columns. D1 (K K^T | Q K^T) and D6 (U'0^T | Z^T of the block substitution) share
+// columns: D1 is consumed before D6 is produced. V^T (identity MMA) lands in the U'd^T columns
+// before they are reused; K^T (identity MMA, GDN) and then U'1^T land in the P U' accumulator
+// columns before MMA4 overwrites them.
 constexpr uint32_t COL_S = 0, COL_D2 = 128, COL_RU = 256, COL_RUD = 320, COL_D1 = 384,
                    COL_D6 = 384, COL_D4 = 448;
 constexpr uint32_t TMEM_COLS = 512;
@@ -56,16 +57,14 @@ constexpr uint32_t SM_V = SM_KQ + 32768;         // bf16 SW128 [64][128]
 constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: K | Q][128] (KDA: scaled)
 constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t]: K^T (GDN) / Kdec^T (KDA)
 constexpr uint32_t SM_P = SM_KDT + 32768;        // tf32 SW128 [64 t][64 i]
-constexpr uint32_t SM_T = SM_P + 16384;          // tf32 SW128 [64 t][64 i]
-constexpr uint32_t SM_ID = SM_T + 16384;         // bf16 SW128 [64][64] identity
+constexpr uint32_t SM_T00 = SM_P + 16384;        // tf32 SW128 [32 t][32 i]  (I + A00)^{-1}
+constexpr uint32_t SM_T11 = SM_T00 + 4096;       // tf32 SW128 [32 t][32 i]  (I + A11)^{-1}
+constexpr uint32_t SM_NA10 = SM_T11 + 4096;      // tf32 SW128 [32 t][32 i]  -A[32 + t][i]
+constexpr uint32_t SM_ID = SM_NA10 + 8192;       // bf16 SW128 [64][64] identity (1024-aligned)
 constexpr uint32_t AT_LD = 68;                   // padded row of the fp32 A^T tile
 constexpr uint32_t SM_AT = SM_ID + 8192;         // fp32 A^T [64 i][68]; later the bf16 O tile
-constexpr uint32_t SL_LD = 36;                   // padded row of the 32x32 solver tiles
-constexpr uint32_t SM_T00 = SM_AT + 64 * AT_LD * 4;   // fp32 T00 [32][36]
-constexpr uint32_t SM_T11T = SM_T00 + 32 * SL_LD * 4; // fp32 T11^T [32][36]
-constexpr uint32_t SM_Y = SM_T11T + 32 * SL_LD * 4;   // fp32 A10 T00 [32][36]
 constexpr uint32_t O_LD = 136;                   // padded row (bf16) of the output staging tile
-constexpr uint32_t SM_SMALL = SM_Y + 32 * SL_LD * 4;
+constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_LD * 4;
 // small region (floats)
 constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 256,
                    SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704 /* [NQ][128] */,
@@ -518,6 +517,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 } else {
 #pragma unroll
                     for (int ii = 0; ii < 16; ++ii) atp[(i0 + ii) * AT_LD + r] = v[ii];
+                    if (r >= 32 && i0 < 32) {  // -A10, the coupling of the two 32-token halves
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<float4 *>(sm + SM_NA10 + tc::sw128_offset(r - 32, i0 + q4 * 4, 32, 4)) =
+                                make_float4(tc::to_tf32(-v[q4 * 4]), tc::to_tf32(-v[q4 * 4 + 1]),
+                                            tc::to_tf32(-v[q4 * 4 + 2]), tc::to_tf32(-v[q4 * 4 + 3]));
+                    }
                 }
                 if (!KDA) {
                     // K^T[c][t] (exact in tf32) -> the [c][t] tile; columns t >= n zeroed
@@ -539,70 +545,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 issue_mma2();
             }
 
-            // ---------------- T = (I + A)^{-1} in 32x32 blocks, fp32 on CUDA cores:
-            //   T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} by forward substitution (8 threads per
-            //   column, rows 8m + p), then T10 = -T11 (A10 T00) as two 32x32x32 products.
+            // ---------------- T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} (the two 32-token
+            //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores, 8
+            //   threads per column (rows 8m + p). The coupling block is applied by the tensor
+            //   core as a block substitution: U'0 = R0 T00^T, U'1 = (R1 - U'0 A10^T) T11^T.
             {
-                float *t00 = reinterpret_cast<float *>(sm + SM_T00);
-                float *t11t = reinterpret_cast<float *>(sm + SM_T11T);
-                float *ys = reinterpret_cast<float *>(sm + SM_Y);
-                {
-                    const int b = warp >> 3, o = 32 * b;
-                    const int jj = 4 * (warp & 7) + (lane >> 3), p = lane & 7;
-                    float x[4];
+                const int b = warp >> 3, o = 32 * b;
+                const int jj = 4 * (warp & 7) + (lane >> 3), p = lane & 7;
+                float x[4];
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) x[m] = (8 * m + p == jj) ? 1.f : 0.f;
-                    const float *ab = atp + o * AT_LD + o + p;  // ab[i*AT_LD + 8m] = A[o+8m+p][o+i]
+                for (int m = 0; m < 4; ++m) x[m] = (8 * m + p == jj) ? 1.f : 0.f;
+                const float *ab = atp + o * AT_LD + o + p;  // ab[i*AT_LD + 8m] = A[o+8m+p][o+i]
 #pragma unroll
-                    for (int i = 0; i < 31; ++i) {
-                        const int m0 = i >> 3;
-                        const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~7) | (i & 7));
-                        {
-                            const float nx = fmaf(-ab[i * AT_LD + 8 * m0], xi, x[m0]);
-                            x[m0] = (p > (i & 7)) ? nx : x[m0];
-                        }
-#pragma unroll
-                        for (int m = m0 + 1; m < 4; ++m) x[m] = fmaf(-ab[i * AT_LD + 8 * m], xi, x[m]);
+                for (int i = 0; i < 31; ++i) {
+                    const int m0 = i >> 3;
+                    const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~7) | (i & 7));
+                    {
+                        const float nx = fmaf(-ab[i * AT_LD + 8 * m0], xi, x[m0]);
+                        x[m0] = (p > (i & 7)) ? nx : x[m0];
                     }
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int t = 8 * m + p;
-                        st_tf32(sm, SM_T + tc::sw128_offset(o + t, o + jj, 64, 4), x[m]);
-                        if (b == 0) {
-                            st_tf32(sm, SM_T + tc::sw128_offset(t, 32 + jj, 64, 4), 0.f);  // T01 = 0
-                            t00[t * SL_LD + jj] = x[m];
-                        } else {
-                            t11t[jj * SL_LD + t] = x[m];
-                        }
-                    }
+                    for (int m = m0 + 1; m < 4; ++m) x[m] = fmaf(-ab[i * AT_LD + 8 * m], xi, x[m]);
                 }
-                __syncthreads();
-                const int jc = lane, tq = warp;  // output rows 2tq, 2tq+1; column jc
-                {   // Y = A10 T00, A10[t][i] = A[32 + t][i]
-                    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 a2 = *reinterpret_cast<const float2 *>(atp + i * AT_LD + 32 + 2 * tq);
-                        const float tv = t00[i * SL_LD + jc];
-                        acc0 = fmaf(a2.x, tv, acc0);
-                        acc1 = fmaf(a2.y, tv, acc1);
-                    }
-                    ys[(2 * tq) * SL_LD + jc] = acc0;
-                    ys[(2 * tq + 1) * SL_LD + jc] = acc1;
-                }
-                __syncthreads();
-                {   // T10 = -T11 Y
-                    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 t2 = *reinterpret_cast<const float2 *>(t11t + i * SL_LD + 2 * tq);
-                        const float yv = ys[i * SL_LD + jc];
-                        acc0 = fmaf(t2.x, yv, acc0);
-                        acc1 = fmaf(t2.y, yv, acc1);
-                    }
-                    st_tf32(sm, SM_T + tc::sw128_offset(32 + 2 * tq, jc, 64, 4), -acc0);
-                    st_tf32(sm, SM_T + tc::sw128_offset(32 + 2 * tq + 1, jc, 64, 4), -acc1);
-                }
+                const uint32_t tile = b == 0 ? SM_T00 : SM_T11;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    st_tf32(sm, tile + tc::sw128_offset(8 * m + p, jj, 32, 4), x[m]);
             }
             tc::fence_async_smem();
             __syncthreads();
@@ -638,6 +606,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 #pragma unroll
                 for (int ii = 0; ii < D32; ++ii) sv[ii] *= KDA ? sf[SF_EL + c0 + ii] : egL;
                 tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);  // Z = R1
 #pragma unroll
                 for (int g = 0; g < D32 / 16; ++g)
                     tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
@@ -646,15 +615,62 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             tc::fence_before_sync();
             __syncthreads();
 
-            // ---------------- U'^T = R^T T^T
+            // ---------------- U'0^T = R0^T T00^T
+            constexpr uint32_t id32 = tc::idesc(128, 32, tc::FMT_TF32);
             if (warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
-                constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_TF32);
 #pragma unroll
-                for (uint32_t kk = 0; kk < 8; ++kk) {
-                    const uint64_t bd = tc::sdesc_sw128((sb + SM_T) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
-                    tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8, bd, id, kk > 0);
-                }
+                for (uint32_t kk = 0; kk < 4; ++kk)
+                    tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8,
+                                    tc::sdesc_sw128((sb + SM_T00) + kk * 32u), id32, kk > 0);
+                tc::mma_commit(bar_b);
+            }
+            wait_bar(bar_b, phase_b);
+            if (!sync_ok(err)) break;
+            // U'0^T rounded to tf32 (A operand of the coupling MMA; also the final U'0^T)
+            {
+                const int c8 = 8 * part;
+                float v[8];
+                tc::tmem_ld8(tc::tmem_addr(tm, lq, COL_D6 + c8), v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) v[ii] = tc::to_tf32(v[ii]);
+                tc::tmem_st8(tc::tmem_addr(tm, lq, COL_RU + c8), v);
+                tc::tmem_wait_st();
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+            // ---------------- Z^T = R1^T - U'0^T A10^T (accumulated onto R1^T)
+            if (warp == 0 && tc::elect_one()) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (uint32_t kk = 0; kk < 4; ++kk)
+                    tc::mma_tf32_ts(tm + COL_D6 + 32, tm + COL_RU + kk * 8,
+                                    tc::sdesc_sw128((sb + SM_NA10) + kk * 32u), id32, 1);
+                tc::mma_commit(bar_b);
+            }
+            wait_bar(bar_b, phase_b);
+            if (!sync_ok(err)) break;
+            // Z^T rounded to tf32 -> the R1 columns (A operand of the last MMA)
+            {
+                const int c8 = 8 * part;
+                float v[8];
+                tc::tmem_ld8(tc::tmem_addr(tm, lq, COL_D6 + 32 + c8), v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) v[ii] = tc::to_tf32(v[ii]);
+                tc::tmem_st8(tc::tmem_addr(tm, lq, COL_RU + 32 + c8), v);
+                tc::tmem_wait_st();
+            }
+            tc::fence_before_sync();
+            __syncthreads();
+            // ---------------- U'1^T = Z^T T11^T  (into the P U' accumulator columns 0..31)
+            if (warp == 0 && tc::elect_one()) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (uint32_t kk = 0; kk < 4; ++kk)
+                    tc::mma_tf32_ts(tm + COL_D4, tm + COL_RU + 32 + kk * 8,
+                                    tc::sdesc_sw128((sb + SM_T11) + kk * 32u), id32, kk > 0);
                 tc::mma_commit(bar_b);
             }
             wait_bar(bar_b, phase_b);
@@ -662,16 +678,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
             // ------ U'^T -> TMEM (tf32); GDN also U'^T diag(e^{gc_L - gc}) for the state update
             {
-                const int t0c = C16 * part;
+                const int t0c = C16 * part;  // 16 columns: U'0 (rounded, in RU) or U'1 (D4)
                 float v[16], w[16];
-                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);
+                if (t0c < 32) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                else tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c - 32), v);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
-                    w[ii] = KDA ? 0.f : tc::to_tf32(v[ii] * sf[SF_EGL + t0c + ii]);
                     v[ii] = tc::to_tf32(v[ii]);
+                    w[ii] = KDA ? 0.f : tc::to_tf32(v[ii] * sf[SF_EGL + t0c + ii]);
                 }
-                tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
                 if (!KDA) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RUD + t0c), w);
             }
             tc::tmem_wait_st();
