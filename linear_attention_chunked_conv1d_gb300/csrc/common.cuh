@@ -43,6 +43,35 @@ template <> struct Vec16<__nv_bfloat16> {
     }
 };
 
+// 4 activations per access (16 bytes of fp32, 8 bytes of bf16), widened to fp32. The
+// elementwise front-end kernels use it so that both dtypes reduce in the same order.
+template <typename T> struct Vec4;
+
+template <> struct Vec4<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void load(const float *p, float *f) { Vec16<float>::load(p, f); }
+    __device__ __forceinline__ static void store(float *p, const float *f) { Vec16<float>::store(p, f); }
+};
+
+template <> struct Vec4<__nv_bfloat16> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *f) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        f[0] = __uint_as_float(v.x << 16);
+        f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+        f[2] = __uint_as_float(v.y << 16);
+        f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    }
+    __device__ __forceinline__ static void store(__nv_bfloat16 *p, const float *f) {
+        uint2 v;
+        __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+        __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+        v.x = *reinterpret_cast<uint32_t *>(&a);
+        v.y = *reinterpret_cast<uint32_t *>(&b);
+        *reinterpret_cast<uint2 *>(p) = v;
+    }
+};
+
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 template <typename T> __device__ __forceinline__ T from_f(float x);

@@ -6,8 +6,8 @@
 // "split_prefill.rs", LayerSplitPrefill::prefill_phase1_conv1d_one (conv over one request's
 // tokens of a batched prefill, advancing that request's conv state).
 //
-// GB300 design: the op is HBM-bound elementwise work, so each thread owns one 16-byte vector
-// of channels (8 bf16 / 4 fp32) and a run of up to ROWS consecutive tokens of ONE stream,
+// GB300 design: the op is HBM-bound elementwise work, so each thread owns 4 channels (an 8-byte
+// bf16 / 16-byte fp32 vector) and a run of up to ROWS consecutive tokens of ONE stream,
 // keeping the kernel-1 previous rows in registers as a sliding window: x is read once (plus
 // kernel-1 halo rows per run, served by L2) and out written once, with coalesced 16-byte
 // accesses. Runs are aligned to stream starts (stream s owns run slots floor(cu[s]/ROWS) + s
@@ -35,13 +35,13 @@ __device__ __forceinline__ int conv_run_base(const int32_t *cu, int s) {
 __device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
 
 template <typename T, int K, int HD>
-__global__ void __launch_bounds__(CONV_THREADS, 4)
+__global__ void __launch_bounds__(CONV_THREADS, 8)
 conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                    const T *__restrict__ x, const T *__restrict__ w,
                    const T *__restrict__ bias, T *__restrict__ out,
                    const int32_t *__restrict__ cu, int B, int total, int C, int64_t xs,
                    int64_t os, int n_l2, float eps, int *status) {
-    using V = Vec16<T>;
+    using V = Vec4<T>;
     constexpr int N = V::N;
     constexpr int LPH = HD > 0 ? HD / N : 1;  // lanes per head
     const int cv = blockIdx.y * CONV_THREADS + threadIdx.x;
@@ -162,7 +162,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                 for (int off = LPH / 2; off > 0; off >>= 1)
                     ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 if (do_l2) {
-                    const float inv = 1.f / sqrtf(ss + eps);
+                    const float inv = rsqrtf(ss + eps);
 #pragma unroll
                     for (int e = 0; e < N; ++e) y[e] *= inv;
                 }
@@ -182,7 +182,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 
 template <typename T, int K, int HD>
 static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
-    constexpr int N = Vec16<T>::N;
+    constexpr int N = Vec4<T>::N;
     int nvec = a.channels / N;
     // Run slots: single stream ceil(total/ROWS); varlen floor(total/ROWS) + B covers every
     // stream's runs (stream s starts at slot floor(cu[s]/ROWS) + s).

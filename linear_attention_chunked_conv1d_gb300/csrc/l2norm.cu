@@ -4,10 +4,10 @@
 // q|k heads x tokens, one head_dim vector per block there, eps = cfg.l2_eps, row stride = conv
 // dim); "split_prefill.rs", LayerSplitPrefill::prefill_phase1_l2_batched.
 //
-// GB300 design: HBM-bound. A group of head_dim/VEC lanes (16 lanes for bf16 d=128) owns one
-// (token, head) vector, each lane one 16-byte load; the sum of squares is reduced with
-// xor-shuffles inside the group, so 256-thread blocks cover 16 heads with fully coalesced
-// 16-byte reads and writes and no shared memory.
+// GB300 design: HBM-bound. A group of head_dim/4 lanes (32 lanes for d = 128) owns one
+// (token, head) vector, each lane 4 channels; the sum of squares is reduced with xor-shuffles
+// inside the group (the same order as the fused conv + L2 kernel, which gives identical bits),
+// with coalesced reads and writes and no shared memory.
 #include "common.cuh"
 #include "launch.h"
 
@@ -18,7 +18,7 @@ constexpr int L2_THREADS = 256;
 template <typename T, int HD>
 __global__ void __launch_bounds__(L2_THREADS)
 l2norm_heads_kernel(T *__restrict__ x, int t, int n_heads, int64_t rs, float eps) {
-    using V = Vec16<T>;
+    using V = Vec4<T>;
     constexpr int N = V::N;
     constexpr int LPH = HD / N;  // lanes per head vector (power of two, <= 32)
     static_assert(LPH >= 1 && LPH <= 32 && (LPH & (LPH - 1)) == 0, "lanes per head");
@@ -38,7 +38,7 @@ l2norm_heads_kernel(T *__restrict__ x, int t, int n_heads, int64_t rs, float eps
 #pragma unroll
     for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     if (!active) return;
-    const float inv = 1.f / sqrtf(ss + eps);
+    const float inv = rsqrtf(ss + eps);
 #pragma unroll
     for (int e = 0; e < N; ++e) f[e] *= inv;
     V::store(p, f);
@@ -46,7 +46,7 @@ l2norm_heads_kernel(T *__restrict__ x, int t, int n_heads, int64_t rs, float eps
 
 template <typename T, int HD>
 static cudaError_t launch_l2_t(const L2Args &a, cudaStream_t st) {
-    constexpr int LPH = HD / Vec16<T>::N;
+    constexpr int LPH = HD / Vec4<T>::N;
     constexpr int per_block = L2_THREADS / LPH;
     int64_t groups = (int64_t)a.t * a.n_heads;
     unsigned blocks = (unsigned)((groups + per_block - 1) / per_block);
