@@ -167,6 +167,29 @@ int la_gdn_prefill_varlen(const uint64_t *h_state_ptrs, const void *q, const voi
                           int64_t k_stride, int64_t v_stride, float scale, int dtype,
                           void *workspace, size_t workspace_bytes, uint64_t stream);
 
+/* GDN varlen like la_gdn_prefill_varlen, for callers that cannot allocate device memory: it
+ * takes no workspace and allocates nothing. Some callers cannot call cudaMalloc or grow a pool
+ * at the moment they run this layer (an engine whose device memory is fully carved up by its
+ * own allocator, a plugin with a fixed call signature that has nowhere to pass a workspace,
+ * code that must not allocate while other work is being captured or replayed); this call lets
+ * them still use the tensor-core path. The paper has no counterpart: it is a library service.
+ *  - Scratch: a fixed array inside the library's device image (about 17 KB), held on every GPU
+ *    that loads the library until the process exits. It serves at most 4096 streams per call;
+ *    more is refused with LA_ERR_UNSUPPORTED before any launch.
+ *  - Covers bf16 activations with dk = dv = 128 (the tensor-core kernel), else
+ *    LA_ERR_UNSUPPORTED. All other arguments and errors are those of la_gdn_prefill_varlen.
+ *  - Shared state: every call on a device uses the same scratch; the call re-initialises what
+ *    must start at zero, but two calls whose work overlaps on the GPU (different streams, no
+ *    ordering between them) race and give wrong results. Order them on one stream or by events.
+ *  - The first call on each device looks up the scratch address (a host-side query, no
+ *    allocation); make that first call before any stream capture on that device. */
+int la_gdn_prefill_varlen_noalloc(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                                  const void *v, const float *g, const float *beta, void *out,
+                                  const int32_t *cu_seqlens, int B, int total_tokens,
+                                  int max_seqlen, int max_tokens, int Hk, int Hv, int dk, int dv,
+                                  int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                  float scale, uint64_t stream);
+
 /* KDA (per-channel gate) over one stream (cu_seqlens == NULL: tokens 0..total_tokens-1, B = 1)
  * or B varlen streams. "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill.
  * gate [total_tokens][Hv][dk] fp32 log-decay per k-channel.

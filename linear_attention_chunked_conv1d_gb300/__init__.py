@@ -20,7 +20,8 @@ __all__ = [
     "LinAttnError", "LA_F32", "LA_BF16", "abi_version", "last_error", "device_status",
     "conv1d_silu_prefill", "conv1d_silu_prefill_varlen", "conv1d_silu_l2_prefill",
     "l2norm_heads",
-    "prefill_workspace_bytes", "gdn_prefill_batched", "gdn_prefill_varlen", "kda_prefill",
+    "prefill_workspace_bytes", "gdn_prefill_batched", "gdn_prefill_varlen",
+    "gdn_prefill_varlen_noalloc", "kda_prefill",
     "pointer_array", "library_path",
 ]
 
@@ -60,6 +61,9 @@ _SIGS = {
     "la_gdn_prefill_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                                _i32, _i32, _i32, _i32, _i64, _i64, _i64, _f32, _i32, _vp, _sz,
                                _u64], ctypes.c_int),
+    "la_gdn_prefill_varlen_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                       _i32, _i32, _i32, _i32, _i32, _i32, _i64, _i64, _i64,
+                                       _f32, _u64], ctypes.c_int),
     "la_kda_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i32, _i64, _i64, _i64, _f32, _f32, _i32, _vp, _sz, _u64],
                        ctypes.c_int),
@@ -212,6 +216,23 @@ def gdn_prefill_varlen(h_state_ptrs, q, k, v, g, beta, out, cu_seqlens, *, max_s
         max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(q),
         _row_stride(k), _row_stride(v), float(scale), _dtype_code(q), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def gdn_prefill_varlen_noalloc(h_state_ptrs, q, k, v, g, beta, out, cu_seqlens, *, max_seqlen,
+                               Hk, Hv, dk, dv, total_tokens=None, scale=None, max_tokens=None,
+                               stream=None) -> None:
+    """gdn_prefill_varlen without a workspace, for callers that cannot allocate device memory:
+    the library's fixed scratch (up to 4096 streams per call) is used instead. Calls that
+    overlap on the GPU share that scratch and must be ordered; the first call on a device
+    should come before any stream capture there."""
+    B = cu_seqlens.shape[0] - 1
+    total = q.shape[0] if total_tokens is None else total_tokens
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    _check(_load().la_gdn_prefill_varlen_noalloc(
+        _ptr(h_state_ptrs), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(out),
+        _ptr(cu_seqlens), B, total, max_seqlen,
+        max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(q),
+        _row_stride(k), _row_stride(v), float(scale), _stream(stream)))
 
 
 def kda_prefill(h_state_ptrs, q, k, v, gate, beta, out, cu_seqlens=None, *, Hk, Hv, dk, dv,

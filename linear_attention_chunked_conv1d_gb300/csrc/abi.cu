@@ -298,6 +298,43 @@ int la_gdn_prefill_varlen(const uint64_t *h_state_ptrs, const void *q, const voi
     return run_recurrence(a, as_stream(stream));
 }
 
+int la_gdn_prefill_varlen_noalloc(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                                  const void *v, const float *g, const float *beta, void *out,
+                                  const int32_t *cu_seqlens, int B, int total_tokens,
+                                  int max_seqlen, int max_tokens, int Hk, int Hv, int dk, int dv,
+                                  int64_t q_stride, int64_t k_stride, int64_t v_stride,
+                                  float scale, uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "varlen prefill of %d tokens does not fit max_tokens %d",
+                    total_tokens, max_tokens);
+    if (!cu_seqlens) return fail(LA_ERR_ARG, "cu_seqlens is NULL");
+    if (max_seqlen < 1 || max_seqlen > total_tokens)
+        return fail(LA_ERR_ARG, "max_seqlen %d outside 1..total_tokens (%d)", max_seqlen,
+                    total_tokens);
+    if (!uses_tensor_cores(LA_BF16, dk, dv))
+        return fail(LA_ERR_UNSUPPORTED, "the no-allocation call covers bf16 with dk = dv = 128");
+    const int max_streams = la::chunk_tc_static_scratch_max_streams();
+    if (B > max_streams)
+        return fail(LA_ERR_UNSUPPORTED,
+                    "%d streams exceed the %d the library's fixed scratch holds; use "
+                    "la_gdn_prefill_varlen with a caller workspace", B, max_streams);
+    LA_TRY(rec_common(h_state_ptrs, q, k, v, g, beta, out, B, Hk, Hv, dk, dv, q_stride, k_stride,
+                      v_stride, LA_BF16, nullptr, 0, 0));
+    void *scratch = nullptr;
+    size_t scratch_bytes = 0;
+    cudaError_t e = la::chunk_tc_static_scratch(&scratch, &scratch_bytes);
+    if (e != cudaSuccess)
+        return fail(LA_ERR_CUDA, "looking up the fixed scratch: %s", cudaGetErrorString(e));
+    la::RecArgs a{};
+    a.h_ptrs = h_state_ptrs; a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
+    a.cu = cu_seqlens; a.B = B; a.T_each = 0; a.total = total_tokens; a.max_seqlen = max_seqlen;
+    a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.q_stride = q_stride; a.k_stride = k_stride; a.v_stride = v_stride;
+    a.scale = scale; a.pad_fill = 0.f; a.dtype = LA_BF16; a.kda = false;
+    a.workspace = scratch; a.workspace_bytes = scratch_bytes;
+    return run_recurrence(a, as_stream(stream));
+}
+
 int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, const void *v,
                    const float *gate, const float *beta, void *out, const int32_t *cu_seqlens,
                    int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,

@@ -29,6 +29,8 @@
 // Precision: operands that are raw bf16 inputs use kind::f16; operands derived from fp32
 // values (state, T, U', decayed keys) use kind::tf32 with round-to-nearest conversion,
 // accumulation is fp32. Rows at or past a stream's end are removed by selects.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -801,6 +803,40 @@ int sm_count() {
 
 size_t chunk_tc_workspace_bytes(int B) {
     return (size_t)((B + 64 + 63) / 64) * 64 * sizeof(int32_t) + 256;
+}
+
+// ---- Fixed, library-owned scratch for callers that cannot hand the library a workspace.
+// It lives in this file's device memory image: every GPU that loads the library holds it until
+// the process exits, and every call through it shares it (the previous call's contents stay;
+// the stream-order kernel rewrites the order and zeroes the counter at the start of each call).
+constexpr int kStaticScratchStreams = 4096;
+constexpr size_t kStaticScratchBytes =
+    (size_t)((kStaticScratchStreams + 64 + 63) / 64) * 64 * sizeof(int32_t) + 256;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+int chunk_tc_static_scratch_max_streams() { return kStaticScratchStreams; }
+
+// Device address of the scratch array for the current device, looked up once per device (with
+// that device current). Host code may not pass the array's name to a kernel: on the host it is
+// only a stand-in symbol, not a device address.
+cudaError_t chunk_tc_static_scratch(void **ptr, size_t *bytes) {
+    constexpr int kMaxDev = 64;
+    static void *cached[kMaxDev] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        cached[dev] = p;
+    }
+    *ptr = cached[dev];
+    *bytes = kStaticScratchBytes;
+    return cudaSuccess;
 }
 
 bool chunk_tc_supported(const RecArgs &a) {

@@ -55,5 +55,9 @@ cudaError_t launch_chunk_simt(const RecArgs &a, cudaStream_t st);
 bool chunk_tc_supported(const RecArgs &a);
 size_t chunk_tc_workspace_bytes(int B);
 cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st);
+// Library-owned scratch usable in place of a workspace by the tensor-core kernel (at most
+// chunk_tc_static_scratch_max_streams() streams per call).
+int chunk_tc_static_scratch_max_streams();
+cudaError_t chunk_tc_static_scratch(void **ptr, size_t *bytes);
 
 }  // namespace la
