@@ -245,6 +245,24 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------ replicas
+def aggregate(tokens_local: int, ms_local: float, pg=None, device=None):
+    """Whole-job throughput of weak-scaled replicas: every rank processes its own batch; the
+    job takes as long as the slowest rank. Returns (tokens/s over all ranks, max ms, ranks)."""
+    if pg is None:
+        return tokens_local / (ms_local * 1e-3), ms_local, 1
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    n = torch.tensor([float(tokens_local)], dtype=torch.float64, device=device)
+    pg.all_reduce(n, op=pg.ReduceOp.SUM)
+    ms = float(t.item())
+    return float(n.item()) / (ms * 1e-3), ms, pg.get_world_size()
+
+
+def uses_tensor_cores(wl) -> bool:
+    return wl.dtype == "bf16" and wl.d == 128
+
+
 # ------------------------------------------------------------------------------ GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -305,11 +323,7 @@ def main():
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     front_ms = [e[0].elapsed_time(e[1]) for e in ev]
     rec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    value, ms, _ = aggregate(T, sum(step_ms) / len(step_ms), pg, dev)
 
     # ---- end to end through the public API: pinned host inputs in, result out, every step
     x_h = inp["x"].cpu().pin_memory()
@@ -335,11 +349,7 @@ def main():
         out_h.copy_(p.out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_value, e2e_ms, _ = aggregate(T, e0.elapsed_time(e1) / args.steps, pg, dev)
 
     if rank != 0:
         if pg:
@@ -355,12 +365,14 @@ def main():
     hbm = float(peaks["hbm_gbs"])
     B_alg, F_alg = path_algorithmic(wl, lengths)
     t_roof = max(F_alg / (float(peaks["bf16_tflops"]) * 1e12), B_alg / (hbm * 1e9))
-    kernel_file = "chunk_simt.cu"
+    tc = uses_tensor_cores(wl)
+    kernel_file = "chunk_tc.cu" if tc else "chunk_simt.cu"
+    kernel_name = "chunk_tc_kernel" if tc else "chunk_simt_kernel"
     traffic = profiled_traffic(kernel_file, wl.name)
-    tokens_all = T * world
+    launches_per_step = 3 if tc else 2  # fused conv+L2, (stream order), recurrence
     line = {
         "metric": METRIC,
-        "value": tokens_all / (ms * 1e-3),
+        "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -369,19 +381,21 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": wl.dtype,
         "data": "synthetic (seeded; x~N(0,1), conv w~N(0,0.25), h~N(0,0.02), "
                 "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
         "config": {"workload": wl.name, "streams": wl.B, "tokens_per_step": T,
                    "Hk": wl.Hk, "Hv": wl.Hv, "head_dim": wl.d, "variant": wl.variant,
                    "activations": wl.dtype, "states": "f32", "chunk": CHUNK,
+                   "compute": ("tensor cores: bf16 (raw inputs) and tf32 (state-derived) MMAs, "
+                               "fp32 accumulate; CUDA cores fp32" if tc else "CUDA cores fp32"),
                    "l2": "flushed between timed steps (write of a 258 MiB buffer)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
-        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": e2e_value, "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "kernel": "chunk_simt_kernel (recurrence)",
+        "roofline": {"bound": "hbm", "kernel": f"{kernel_name} (recurrence)",
                      "achieved": rec_achieved, "peak": hbm, "unit": "GB/s",
                      "frac": rec_achieved / hbm, "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs",
