@@ -70,7 +70,8 @@ constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_LD * 4;
 // small region (floats)
 constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 256,
                    SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704 /* [NQ][128] */,
-                   SF_WARP = 704 + 128 * NQ, SF_END = SF_WARP + 8;
+                   SF_WARP = 704 + 128 * NQ, SF_RF = SF_WARP + 8, SF_CF = SF_RF + 64,
+                   SF_END = SF_CF + 64;
 constexpr uint32_t SM_BYTES = SM_SMALL + SF_END * 4 + 64;  // + mbarriers, flags, tmem base
 constexpr size_t TC_SMEM = SM_BYTES + 1024;                // alignment slack
 constexpr float LOG2E = 1.4426950408889634f;
@@ -247,8 +248,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         }
         tc::tmem_wait_st();
 
-        // gate and beta of the chunk being computed are fetched one chunk ahead (threads < 64)
+        // gates and beta of the chunk being computed are fetched one chunk ahead: GDN and beta
+        // by threads < 64, the KDA gate tile by every thread (16 rows of its channel)
         float pre_g = 0.f, pre_b = 0.f;
+        float pre_gk[KDA ? C16 : 1];
         auto fetch_gates = [&](int tok, int nn) {
             if (tid < TC_C) {
                 pre_b = tid < nn ? a.beta[(int64_t)(tok + tid) * Hv + j] : 0.f;
@@ -256,6 +259,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
         };
         fetch_gates(t0, min(TC_C, len));
+        if (KDA) {
+            const int nn = min(TC_C, len);
+            const float *gp = a.g + ((int64_t)t0 * Hv + j) * TC_D + row;
+#pragma unroll
+            for (int t = 0; t < C16; ++t) {
+                const int tt = C16 * part + t;
+                pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
+            }
+        }
 
         for (int ch = 0; ch < nch; ++ch) {
             const int tok0 = t0 + ch * TC_C;
@@ -265,12 +277,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             // ---------------- gates
             float gcr[KDA ? C16 : 1];  // KDA: gc[C16*part + t][c], c = row
             if (KDA) {
-                const float *gp = a.g + ((int64_t)tok0 * Hv + j) * TC_D + row;
                 float acc = 0.f;
 #pragma unroll
                 for (int t = 0; t < C16; ++t) {
-                    const int tt = C16 * part + t;
-                    acc += tt < n ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
+                    acc += pre_gk[t];
                     gcr[t] = acc;
                 }
                 sf[SF_CARRY + part * 128 + row] = acc;
@@ -326,8 +336,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             __syncthreads();
             if (!KDA && tid < TC_C) {
                 const float gct = sf[SF_GC + tid], gL = sf[SF_GC + TC_C - 1];
+                const float gm = sf[SF_GC + TC_C / 2 - 1];
                 sf[SF_EG + tid] = __expf(gct);
                 sf[SF_EGL + tid] = __expf(gL - gct);
+                // e^{gc_t - gc_i} = e^{gc_t - gc_m} e^{gc_m - gc_i} (m = row 31): both factors
+                // are bounded by the half-chunk decay range, checked below
+                sf[SF_RF + tid] = __expf(gct - gm);
+                sf[SF_CF + tid] = __expf(gm - gct);
             }
 
             // ---------------- D1 = [K;Q] K^T (KDA: decays split at row 31); GDN also K^T
@@ -387,44 +402,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             // ---- state-MMA operands. GDN: exact tf32 copy of [K;Q] (the gate factors are
             //      applied to the MMA results instead). KDA: [K e^gc ; Q e^gc] and
             //      (K e^{gc_L - gc})^T, thread per (channel, row part).
-            auto stage_state_operands = [&]() {
-                if (!KDA) {
+            auto stage_state_operands = [&]() {  // GDN
 #pragma unroll
-                    for (int m = 0; m < 2048 / TC_THREADS; ++m) {
-                        const int idx = tid + TC_THREADS * m;  // 0..2047 chunks of 8 elements
-                        const int r = idx >> 4, cj = idx & 15;
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
-                        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                        float f[8];
+                for (int m = 0; m < 2048 / TC_THREADS; ++m) {
+                    const int idx = tid + TC_THREADS * m;  // 0..2047 chunks of 8 elements
+                    const int r = idx >> 4, cj = idx & 15;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    float f[8];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            f[2 * e] = __uint_as_float(w4[e] << 16);
-                            f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
-                        }
-                        *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8, 128, 4)) =
-                            make_float4(f[0], f[1], f[2], f[3]);
-                        *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8 + 4, 128, 4)) =
-                            make_float4(f[4], f[5], f[6], f[7]);
+                    for (int e = 0; e < 4; ++e) {
+                        f[2 * e] = __uint_as_float(w4[e] << 16);
+                        f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
                     }
-                } else {
-                    const int c = row;
-                    const float gLc = sf[SF_GL + c];
-                    float kd[4];
-#pragma unroll
-                    for (int t = 0; t < C16; ++t) {
-                        const int tt = C16 * part + t;
-                        const bool valid = tt < n;
-                        const float kv = ld_bf16(sm, w_kq.at(tt));
-                        const float qv = ld_bf16(sm, w_kq.at(64 + tt));
-                        const float eg = __expf(gcr[t]), egl = __expf(gLc - gcr[t]);  // both <= 1
-                        st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
-                        st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
-                        kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
-                        if ((t & 3) == 3) {
-                            *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
-                                make_float4(kd[0], kd[1], kd[2], kd[3]);
-                        }
-                    }
+                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8, 128, 4)) =
+                        make_float4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8 + 4, 128, 4)) =
+                        make_float4(f[4], f[5], f[6], f[7]);
                 }
                 tc::fence_async_smem();
             };
@@ -495,20 +489,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             {
                 const int r = row & 63;
                 const bool isq = row >= 64;
-                const float gct2 = KDA ? 0.f : sf[SF_GC2 + r];
                 const float bt = sf[SF_BETA + r];
                 const bool rv = r < n;
                 const int i0 = C16 * part;
+                // GDN decays: row factor x column factor when the half-chunk range allows it
+                // (uniform per chunk), else the exact exponential of the difference
+                const float gm_ = KDA ? 0.f : sf[SF_GC + TC_C / 2 - 1];
+                const bool split_ok = KDA || (-gm_ <= 80.f && gm_ - sf[SF_GC + TC_C - 1] <= 80.f);
+                const float gct2 = KDA ? 0.f : sf[SF_GC2 + r];
+                const float rowf = (KDA ? 1.f : sf[SF_RF + r]) * (isq ? 1.f : bt);
                 float v[16], kt[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D1 + i0), v);
                 if (!KDA) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + i0), kt);
                 tc::tmem_wait_ld();
+                if (KDA || split_ok) {
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) {
-                    const int i = i0 + ii;
-                    const float dec = KDA ? 1.f : tc::ex2(fminf(gct2 - sf[SF_GC2 + i], 0.f));
-                    v[ii] = isq ? ((rv && i <= r) ? dec * v[ii] : 0.f)
-                                : ((rv && i < r) ? bt * dec * v[ii] : 0.f);
+                    for (int ii = 0; ii < 16; ++ii) {
+                        const int i = i0 + ii;
+                        const float f = KDA ? rowf : rowf * sf[SF_CF + i];
+                        const bool keep = rv && (isq ? i <= r : i < r);
+                        v[ii] = keep ? f * v[ii] : 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int ii = 0; ii < 16; ++ii) {
+                        const int i = i0 + ii;
+                        const float dec = tc::ex2(fminf(gct2 - sf[SF_GC2 + i], 0.f));
+                        v[ii] = isq ? ((rv && i <= r) ? dec * v[ii] : 0.f)
+                                    : ((rv && i < r) ? bt * dec * v[ii] : 0.f);
+                    }
                 }
                 if (isq) {
 #pragma unroll
@@ -543,7 +552,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             __syncthreads();
 
             if (KDA) {  // KDA: the Kl|Ql and Kr buffers are free now
-                stage_state_operands();
+                // [K e^gc ; Q e^gc] and (K e^{gc_L - gc})^T, thread per (channel, row part)
+                const int c = row;
+                const float gLc = sf[SF_GL + c];
+                float kd[4];
+#pragma unroll
+                for (int t = 0; t < C16; ++t) {
+                    const int tt = C16 * part + t;
+                    const bool valid = tt < n;
+                    const float kv = ld_bf16(sm, w_kq.at(tt));
+                    const float qv = ld_bf16(sm, w_kq.at(64 + tt));
+                    const float eg = __expf(gcr[t]), egl = __expf(gLc - gcr[t]);  // both <= 1
+                    st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
+                    st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
+                    kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
+                    if ((t & 3) == 3) {
+                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
+                            make_float4(kd[0], kd[1], kd[2], kd[3]);
+                    }
+                }
+                tc::fence_async_smem();
                 issue_mma2();
             }
 
@@ -580,6 +608,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
                 fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
+                if (KDA) {
+                    const int nn = min(TC_C, len - (ch + 1) * TC_C);
+                    const float *gp = a.g + ((int64_t)(tok0 + TC_C) * Hv + j) * TC_D + row;
+#pragma unroll
+                    for (int t = 0; t < C16; ++t) {
+                        const int tt = C16 * part + t;
+                        pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
+                    }
+                }
             }
 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})

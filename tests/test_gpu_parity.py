@@ -347,3 +347,16 @@ def test_fused_conv_l2_equals_two_launches_and_oracle(cuda, dtype, hd, lengths):
     else:
         assert bf16_ulp_diff(got, ref) <= 1
     np.testing.assert_array_equal(f64(st2.cpu()), ref_st)
+
+
+def test_gdn_extreme_gates_exact_decay_path(cuda):
+    """Half-chunk decays beyond e^80 (g = -12 per token): the tensor-core kernel must use the
+    exact pairwise decay instead of the row x column factorisation, and still match."""
+    inp = recurrence_inputs([200, 77], 2, 4, 128, dtype="bf16", seed=93)
+    g = inp["g"].clone()
+    g[:, 1] = -12.0
+    g[60:140, 2] = -30.0
+    inp["g"] = g
+    o, h = run_rec(cuda, inp, 2, 4, 128, kda=False, mode="varlen")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(h).all()
+    check_parity(inp, o, h, 2, 4, 128, False, "bf16")
