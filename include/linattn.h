@@ -205,6 +205,43 @@ int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, c
                    float scale, float pad_fill, int dtype, void *workspace,
                    size_t workspace_bytes, uint64_t stream);
 
+/* The whole prefill of one GDN or KDA layer in one call: causal depthwise conv1d + SiLU over
+ * the carried conv state, L2 norm of every q and k head row, then the chunked recurrence, with
+ * the conv output kept on chip (it never reaches HBM). Results are those of
+ * la_conv1d_silu_l2_prefill followed by la_gdn_prefill_batched / la_gdn_prefill_varlen /
+ * la_kda_prefill on the same inputs (bit for bit: the same arithmetic in the same order).
+ * "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill (conv_prefill, l2,
+ * chunk_prepare and chunk_scan launches); "split_prefill.rs", prefill_phase1_conv1d_one,
+ * prefill_phase1_l2_batched and prefill_gdn_full_batched(_fla_varlen).
+ *
+ * conv_state_ptrs DEVICE array of B device pointers (each 16-byte aligned); pointer s -> conv
+ *               state of stream s, [conv_kernel - 1][cd] in x's dtype, oldest row first; read
+ *               and advanced in place. May be NULL when conv_kernel == 1.
+ * h_state_ptrs  as for the recurrence calls ([Hv][dk][dv] fp32 per stream, in place).
+ * x             [total_tokens][x_stride] pre-conv rows, cd = 2*Hk*dk + Hv*dv channels packed
+ *               [q heads | k heads | v heads]; 16-byte aligned, x_stride a multiple of 16 bytes.
+ * conv_w        [cd][conv_kernel] (x's dtype), tap conv_kernel-1 multiplies the current token.
+ * conv_bias     [cd] (x's dtype) or NULL.
+ * g, beta       GDN (kda == 0): g [total_tokens][Hv]; KDA (kda == 1): g [total_tokens][Hv][dk];
+ *               beta [total_tokens][Hv]; fp32.
+ * out           [total_tokens][Hv][dv] (x's dtype, contiguous).
+ * cu_seqlens    DEVICE int32 [B + 1], or NULL for B streams of total_tokens / B tokens each
+ *               (total_tokens must then be a multiple of B).
+ * l2_eps        x / sqrt(sum x^2 + l2_eps) per q/k head row.
+ * pad_fill      KDA: value of the q/k tile rows past a stream's end before masking (as
+ *               la_kda_prefill); results do not depend on it. GDN ignores it (zeros there).
+ * workspace     at least la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype).
+ * Covers bf16 activations with dk = dv = 128 (the tensor-core kernel) and conv_kernel 1..4;
+ * anything else is LA_ERR_UNSUPPORTED (use the separate calls). Count rule:
+ * 1 <= total_tokens <= max_tokens. A zero-length stream leaves both of its states unchanged. */
+int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs,
+                     const void *x, const void *conv_w, const void *conv_bias, int conv_kernel,
+                     const float *g, const float *beta, void *out, const int32_t *cu_seqlens,
+                     int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,
+                     int dk, int dv, int64_t x_stride, float l2_eps, float scale, float pad_fill,
+                     int kda, int dtype, void *workspace, size_t workspace_bytes,
+                     uint64_t stream);
+
 #ifdef __cplusplus
 }
 #endif

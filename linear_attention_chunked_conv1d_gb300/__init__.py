@@ -67,6 +67,9 @@ _SIGS = {
     "la_kda_prefill": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i32, _i64, _i64, _i64, _f32, _f32, _i32, _vp, _sz, _u64],
                        ctypes.c_int),
+    "la_prefill_front": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                          _i32, _i32, _i32, _i32, _i32, _i64, _f32, _f32, _f32, _i32, _i32, _vp,
+                          _sz, _u64], ctypes.c_int),
 }
 
 _lib = None
@@ -249,4 +252,27 @@ def kda_prefill(h_state_ptrs, q, k, v, gate, beta, out, cu_seqlens=None, *, Hk, 
         _ptr(cu_seqlens), B, total, max_seqlen,
         max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(q),
         _row_stride(k), _row_stride(v), float(scale), float(pad_fill), _dtype_code(q),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def prefill_front(conv_state_ptrs, h_state_ptrs, x, conv_w, gate, beta, out, cu_seqlens=None, *,
+                  B=None, Hk, Hv, dk, dv, kda, conv_bias=None, max_seqlen=None,
+                  total_tokens=None, l2_eps=1e-6, scale=None, pad_fill=0.0, max_tokens=None,
+                  workspace=None, stream=None) -> None:
+    """conv1d + SiLU + q|k L2 + recurrence of one layer in one launch, from the pre-conv rows
+    x [tok][2*Hk*dk + Hv*dv]. cu_seqlens None: B equal streams (B defaults to 1)."""
+    if cu_seqlens is not None:
+        B = cu_seqlens.shape[0] - 1
+    elif B is None:
+        B = 1
+    total = x.shape[0] if total_tokens is None else total_tokens
+    max_seqlen = (total // B if cu_seqlens is None else total) if max_seqlen is None else max_seqlen
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _, K = conv_w.shape
+    _check(_load().la_prefill_front(
+        _ptr(conv_state_ptrs), _ptr(h_state_ptrs), _ptr(x), _ptr(conv_w), _ptr(conv_bias), K,
+        _ptr(gate), _ptr(beta), _ptr(out), _ptr(cu_seqlens), B, total, max_seqlen,
+        max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(x),
+        float(l2_eps), float(scale), float(pad_fill), 1 if kda else 0, _dtype_code(x),
         _ptr(workspace), ws_bytes, _stream(stream)))

@@ -247,7 +247,8 @@ size_t la_prefill_workspace_bytes(int B, int total_tokens, int Hk, int Hv, int d
                                   int dtype) {
     (void)total_tokens; (void)Hk; (void)Hv;
     if (B < 1) return 0;
-    return uses_tensor_cores(dtype, dk, dv) ? la::chunk_tc_workspace_bytes(B) : 0;
+    if (Hk < 0) Hk = 0;
+    return uses_tensor_cores(dtype, dk, dv) ? la::chunk_tc_workspace_bytes(B, Hk) : 0;
 }
 
 int la_gdn_prefill_batched(const uint64_t *h_state_ptrs, const void *q, const void *k,
@@ -363,6 +364,69 @@ int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, c
     a.scale = scale; a.pad_fill = pad_fill; a.dtype = dtype; a.kda = true;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     return run_recurrence(a, as_stream(stream));
+}
+
+int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs,
+                     const void *x, const void *conv_w, const void *conv_bias, int conv_kernel,
+                     const float *g, const float *beta, void *out, const int32_t *cu_seqlens,
+                     int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,
+                     int dk, int dv, int64_t x_stride, float l2_eps, float scale, float pad_fill,
+                     int kda, int dtype, void *workspace, size_t workspace_bytes,
+                     uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "prefill of %d tokens does not fit max_tokens %d", total_tokens,
+                    max_tokens);
+    LA_TRY(check_dtype(dtype));
+    if (kda != 0 && kda != 1) return fail(LA_ERR_ARG, "kda must be 0 (GDN) or 1 (KDA)");
+    if (B < 1) return fail(LA_ERR_ARG, "B must be >= 1 (got %d)", B);
+    if (Hk < 1 || Hv < 1) return fail(LA_ERR_ARG, "Hk and Hv must be >= 1 (got %d, %d)", Hk, Hv);
+    if (Hv % Hk) return fail(LA_ERR_ARG, "Hv (%d) is not a multiple of Hk (%d)", Hv, Hk);
+    if (!uses_tensor_cores(dtype, dk, dv))
+        return fail(LA_ERR_UNSUPPORTED,
+                    "the fused prefill covers bf16 with dk = dv = 128; use the separate calls");
+    if (conv_kernel < 1 || conv_kernel > 4)
+        return fail(LA_ERR_UNSUPPORTED, "conv kernel %d outside the compiled 1..4", conv_kernel);
+    int T_each = 0;
+    if (!cu_seqlens) {
+        if (total_tokens % B)
+            return fail(LA_ERR_ARG, "cu_seqlens NULL: total_tokens (%d) is not a multiple of B (%d)",
+                        total_tokens, B);
+        T_each = total_tokens / B;
+        max_seqlen = T_each;
+    } else if (max_seqlen < 1 || max_seqlen > total_tokens) {
+        return fail(LA_ERR_ARG, "max_seqlen %d outside 1..total_tokens (%d)", max_seqlen,
+                    total_tokens);
+    }
+    const int64_t cd = (int64_t)(2 * Hk) * dk + (int64_t)Hv * dv;
+    if (!h_state_ptrs) return fail(LA_ERR_ARG, "h_state_ptrs is NULL");
+    if (conv_kernel > 1 && !conv_state_ptrs) return fail(LA_ERR_ARG, "conv_state_ptrs is NULL");
+    LA_TRY(check_act_ptr(x, "x"));
+    LA_TRY(check_act_ptr(out, "out"));
+    LA_TRY(check_act_ptr(conv_bias, "conv_bias", true));
+    if (!conv_w) return fail(LA_ERR_ARG, "conv_w is NULL");
+    if (!g) return fail(LA_ERR_ARG, "g is NULL");
+    if (!beta) return fail(LA_ERR_ARG, "beta is NULL");
+    LA_TRY(check_stride(x_stride, cd, dtype, "x_stride"));
+    if (x == out) return fail(LA_ERR_ARG, "out may not alias x");
+    if (!(l2_eps >= 0.f)) return fail(LA_ERR_ARG, "l2_eps must be >= 0");
+    const size_t need = la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype);
+    if (workspace_bytes < need)
+        return fail(LA_ERR_ARG, "workspace of %zu bytes is below the %zu required", workspace_bytes,
+                    need);
+    if (!workspace || !aligned16(workspace))
+        return fail(LA_ERR_ARG, "workspace is NULL or not 16-byte aligned");
+    la::RecArgs a{};
+    a.h_ptrs = h_state_ptrs; a.g = g; a.beta = beta; a.out = out;
+    a.cu = cu_seqlens; a.B = B; a.T_each = T_each; a.total = total_tokens;
+    a.max_seqlen = max_seqlen;
+    a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.scale = scale; a.pad_fill = pad_fill; a.dtype = dtype; a.kda = kda == 1;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.front = true;
+    a.x = x; a.conv_w = conv_w; a.conv_bias = conv_bias; a.conv_state_ptrs = conv_state_ptrs;
+    a.x_stride = x_stride; a.conv_k = conv_kernel; a.l2_eps = l2_eps;
+    a.status = status_ptr();
+    return launch_result(la::launch_chunk_tc(a, as_stream(stream)), "fused prefill (tcgen05) launch");
 }
 
 }  // extern "C"

@@ -26,6 +26,16 @@
 // mid-row split, whose range is checked per chunk; a chunk whose half-chunk decay exceeds
 // e^80 in some channel takes an exact pairwise-exponent path for D1 on the CUDA cores.
 //
+// Fused front end (FRONT): the block also computes its q, k and v tiles, chunk by chunk, from
+// the pre-conv rows x — causal depthwise conv over the carried conv state, SiLU, and the L2
+// norm of each q and k row ("glm5next_kda/prefill.rs", conv_prefill and l2 launches) — so the
+// conv output never reaches HBM. The next chunk's raw rows (64 + 3 halo) are copied into the
+// buffer of the tf32 K|Q tile once the state MMA has read it, and turned into the bf16 tiles
+// while the tensor core runs the state update. Arithmetic and reduction order are those of
+// the conv and L2 kernels, so both paths give identical bits. The conv state of a stream is
+// advanced by the blocks that read it: v channels by their unit, q|k channels by the last of
+// the units sharing that k-head to read the old state (a per-(stream, k-head) count).
+//
 // Precision: operands that are raw bf16 inputs use kind::f16; operands derived from fp32
 // values (state, T, U', decayed keys) use kind::tf32 with round-to-nearest conversion,
 // accumulation is fp32. Rows at or past a stream's end are removed by selects.
@@ -72,7 +82,16 @@ constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 
                    SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704 /* [NQ][128] */,
                    SF_WARP = 704 + 128 * NQ, SF_RF = SF_WARP + 8, SF_CF = SF_RF + 64,
                    SF_END = SF_CF + 64;
-constexpr uint32_t SM_BYTES = SM_SMALL + SF_END * 4 + 64;  // + mbarriers, flags, tmem base
+constexpr uint32_t SM_BARS = SM_SMALL + SF_END * 4;  // mbarriers, flags, tmem base (64 B)
+// fused front end: conv taps (fp32 [3 x 128 channels][4], leading taps zero when kernel < 4)
+// and bias of the unit's q | k | v channels; the raw rows share the tf32 K|Q buffer
+constexpr uint32_t SM_CW = SM_BARS + 64;
+constexpr uint32_t SM_CB = SM_CW + 3 * TC_D * 16;
+constexpr uint32_t SM_RAW = SM_KQG;             // bf16 [67 rows][384 channels]
+constexpr int RAW_ROWS = TC_C + 3;              // chunk + halo of the longest conv (4 taps)
+constexpr uint32_t RAW_LD = 3 * TC_D * 2;       // bytes per raw row
+static_assert(RAW_ROWS * RAW_LD <= 65536, "raw rows fit the K|Q staging buffer");
+constexpr uint32_t SM_BYTES = SM_CB + 3 * TC_D * 4;
 constexpr size_t TC_SMEM = SM_BYTES + 1024;                // alignment slack
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -80,6 +99,7 @@ struct TcParams {
     RecArgs a;
     const int32_t *perm;  // streams sorted by decreasing length
     int *counter;         // unit claim counter (zeroed by the order kernel)
+    int *conv_readers;    // fused front end: [B][Hk] readers of the old conv state so far
     int num_units;
 };
 
@@ -149,13 +169,152 @@ __device__ __forceinline__ void load_v(const RecArgs &a, unsigned char *sm, int 
     }
 }
 
+// ---- fused front end
+// First channel of section sec (0 q, 1 k, 2 v) of a unit within a packed x row.
+__device__ __forceinline__ int front_channel(const RecArgs &a, int sec, int kh, int j) {
+    return sec == 0 ? kh * TC_D : sec == 1 ? (a.Hk + kh) * TC_D : (2 * a.Hk + j) * TC_D;
+}
+
+// Conv taps and bias of the unit's 384 channels -> shared memory (fp32, taps right-aligned).
+__device__ __forceinline__ void load_conv_weights(const RecArgs &a, unsigned char *sm, int kh,
+                                                  int j, int tid) {
+    const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(a.conv_w);
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(a.conv_bias);
+    const int K = a.conv_k;
+    for (int idx = tid; idx < 3 * TC_D; idx += TC_THREADS) {
+        const int ch = front_channel(a, idx / TC_D, kh, j) + idx % TC_D;
+        float tap[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            tap[m] = m >= 4 - K ? __bfloat162float(w[(int64_t)ch * K + m - (4 - K)]) : 0.f;
+        reinterpret_cast<float4 *>(sm + SM_CW)[idx] = make_float4(tap[0], tap[1], tap[2], tap[3]);
+        reinterpret_cast<float *>(sm + SM_CB)[idx] = b ? __bfloat162float(b[ch]) : 0.f;
+    }
+}
+
+// Raw rows of the chunk starting at stream row rel0: raw row rho holds stream row
+// rel0 - 3 + rho of [conv state ; x] (rows before the stream come from the carried state,
+// rows past its end and before the state are zero-filled), q | k | v channels of the unit.
+__device__ __forceinline__ void load_raw(const RecArgs &a, unsigned char *sm,
+                                         const __nv_bfloat16 *state, int t0, int len, int rel0,
+                                         int kh, int j, int tid) {
+    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a.x);
+    const int64_t cd = (int64_t)(2 * a.Hk + a.Hv) * TC_D;
+    const int K1 = a.conv_k - 1;
+    const uint32_t base = tc::smem_u32(sm + SM_RAW);
+    for (int idx = tid; idx < RAW_ROWS * 48; idx += TC_THREADS) {
+        const int rho = idx / 48, cc = idx - rho * 48;  // cc: 16-byte piece, 16 per section
+        const int ch = front_channel(a, cc >> 4, kh, j) + (cc & 15) * 8;
+        const int r = rel0 - 3 + rho;
+        const __nv_bfloat16 *src = x;
+        bool valid;
+        if (r >= 0) {
+            valid = r < len;
+            if (valid) src = x + (int64_t)(t0 + r) * a.x_stride + ch;
+        } else {
+            valid = state != nullptr && K1 + r >= 0;
+            if (valid) src = state + (int64_t)(K1 + r) * cd + ch;
+        }
+        cp_async16(base + rho * RAW_LD + cc * 16, src, valid);
+    }
+}
+
+// q, k, v tiles of a chunk from its raw rows: out[t][c] = SiLU(b[c] + sum_m w[c][m] xh[t-3+m][c])
+// rounded to bf16, then q and k rows scaled by 1/sqrt(sum of squares + eps) and rounded again.
+// Warp w takes rows 4w..4w+3, lane l the channel quad 4l..4l+3 of each section: a section row
+// is one warp, reduced with xor-shuffles in the order of the L2 kernel. Rows >= n get pad (q, k)
+// or zero (v).
+__device__ __forceinline__ void conv_tile(const RecArgs &a, unsigned char *sm, int n, float pad,
+                                          int warp, int lane) {
+    const float4 *cw = reinterpret_cast<const float4 *>(sm + SM_CW);
+    const float *cb = reinterpret_cast<const float *>(sm + SM_CB);
+    const int K = a.conv_k;
+    const int tau0 = 4 * warp;
+    const __nv_bfloat162 pf2 = __float2bfloat162_rn(pad);
+    const uint32_t pfw = *reinterpret_cast<const uint32_t *>(&pf2);
+#pragma unroll 1
+    for (int sec = 0; sec < 3; ++sec) {
+        const int c0 = sec * TC_D + 4 * lane;
+        float wt[4][4], bs[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 wv = cw[c0 + e];
+            wt[e][0] = wv.x; wt[e][1] = wv.y; wt[e][2] = wv.z; wt[e][3] = wv.w;
+            bs[e] = cb[c0 + e];
+        }
+        float xr[7][4];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) {
+            const uint2 raw = *reinterpret_cast<const uint2 *>(sm + SM_RAW + (tau0 + i) * RAW_LD + c0 * 2);
+            xr[i][0] = __uint_as_float(raw.x << 16);
+            xr[i][1] = __uint_as_float(raw.x & 0xFFFF0000u);
+            xr[i][2] = __uint_as_float(raw.y << 16);
+            xr[i][3] = __uint_as_float(raw.y & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int tau = tau0 + q;
+            float y[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float acc = bs[e];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) acc = fmaf(wt[e][m], m >= 4 - K ? xr[q + m][e] : 0.f, acc);
+                y[e] = silu(acc);
+            }
+            if (sec < 2) {
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    y[e] = __bfloat162float(__float2bfloat16_rn(y[e]));
+                    ss = fmaf(y[e], y[e], ss);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float inv = rsqrtf(ss + a.l2_eps);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] *= inv;
+            }
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
+            uint2 packed = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                      *reinterpret_cast<const uint32_t *>(&hi));
+            if (tau >= n) packed = sec < 2 ? make_uint2(pfw, pfw) : make_uint2(0u, 0u);
+            const uint32_t off = sec == 2 ? SM_V + tc::sw128_offset(tau, 4 * lane, 64, 2)
+                                          : SM_KQ + tc::sw128_offset((sec == 0 ? 64 : 0) + tau, 4 * lane, 128, 2);
+            *reinterpret_cast<uint2 *>(sm + off) = packed;
+        }
+    }
+}
+
+// New conv state of a stream, rows i < kernel - 1 = stream rows len - (kernel - 1) + i of
+// [old state ; x], for the sections in [sec0, sec1): from the first chunk's raw rows when the
+// stream fits one chunk, else from x.
+__device__ __forceinline__ void write_conv_state(const RecArgs &a, const unsigned char *sm,
+                                                 __nv_bfloat16 *state, int t0, int len, int kh,
+                                                 int j, int sec0, int sec1, int tid) {
+    const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a.x);
+    const int64_t cd = (int64_t)(2 * a.Hk + a.Hv) * TC_D;
+    const int K1 = a.conv_k - 1;
+    const int per = (sec1 - sec0) * 16;
+    for (int idx = tid; idx < K1 * per; idx += TC_THREADS) {
+        const int i = idx / per, cc = sec0 * 16 + idx % per;
+        const int ch = front_channel(a, cc >> 4, kh, j) + (cc & 15) * 8;
+        const int r = len - K1 + i;
+        const uint4 v = len <= TC_C
+                            ? *reinterpret_cast<const uint4 *>(sm + SM_RAW + (r + 3) * RAW_LD + cc * 16)
+                            : *reinterpret_cast<const uint4 *>(x + (int64_t)(t0 + r) * a.x_stride + ch);
+        *reinterpret_cast<uint4 *>(state + (int64_t)i * cd + ch) = v;
+    }
+}
+
 // Block-wide barrier that also reports whether any thread raised the local error flag.
 __device__ __forceinline__ bool sync_ok(volatile int *flag) {
     __syncthreads();
     return *flag == 0;
 }
 
-template <bool KDA>
+template <bool KDA, bool FRONT>
 __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams P) {
     const RecArgs &a = P.a;
     extern __shared__ unsigned char smem_raw[];
@@ -164,12 +323,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                                           ~static_cast<uintptr_t>(1023));
     float *sf = reinterpret_cast<float *>(sm + SM_SMALL);
     float *atp = reinterpret_cast<float *>(sm + SM_AT);
-    uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_SMALL + SF_END * 4);
+    uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_BARS);
     uint64_t *bar_b = bar_a + 1;
-    volatile int *err = reinterpret_cast<volatile int *>(sm + SM_SMALL + SF_END * 4 + 16);
+    volatile int *err = reinterpret_cast<volatile int *>(sm + SM_BARS + 16);
     volatile int *unit_sh = err + 1;
     volatile int *slow_sh = err + 2;
-    uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + SM_SMALL + SF_END * 4 + 32);
+    volatile int *qk_sh = err + 3;
+    uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + SM_BARS + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t lq = tc::tmem_lane_base(warp);  // this warp's TMEM lane quadrant
@@ -218,6 +378,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
     const float scale = a.scale;
     const int Hv = a.Hv, group = a.Hv / a.Hk;
+    // q|k pad rows of the fused front end: pad_fill (KDA); zero for GDN, whose k tile is also
+    // contracted over tokens by the transposing MMA, where a NaN row would reach every column
+    const float pad_qk = KDA ? a.pad_fill : 0.f;
 
     for (;;) {
         __syncthreads();  // everyone has read the previous unit index
@@ -235,8 +398,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         float *hg = reinterpret_cast<float *>(a.h_ptrs[s]) + (int64_t)j * TC_D * TC_D;
         __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) + (int64_t)j * TC_D;
 
-        load_kq(a, sm, t0, min(TC_C, len), kh, tid);
-        load_v(a, sm, t0, min(TC_C, len), j, tid);
+        __nv_bfloat16 *conv_state =
+            FRONT && a.conv_k > 1 ? reinterpret_cast<__nv_bfloat16 *>(a.conv_state_ptrs[s]) : nullptr;
+        if (FRONT) {
+            load_conv_weights(a, sm, kh, j, tid);
+            load_raw(a, sm, conv_state, t0, len, 0, kh, j, tid);
+        } else {
+            load_kq(a, sm, t0, min(TC_C, len), kh, tid);
+            load_v(a, sm, t0, min(TC_C, len), j, tid);
+        }
         cp_async_commit();
         // S[d][c] = H[c][d]: thread (d, part) loads columns c in [D32*part, D32*part + D32)
 #pragma unroll
@@ -247,6 +417,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + D32 * part + g * 16), v);
         }
         tc::tmem_wait_st();
+        if (FRONT) {  // first chunk's q, k, v tiles; advance the conv state
+            cp_async_wait_all();
+            __syncthreads();
+            if (conv_state) {
+                // v channels belong to this unit alone; q|k channels are written by the last
+                // unit of the k-head group to have read the old state
+                if (tid == 0) {
+                    __threadfence();
+                    *qk_sh = atomicAdd(P.conv_readers + s * a.Hk + kh, 1) == group - 1;
+                    __threadfence();
+                }
+                __syncthreads();
+                write_conv_state(a, sm, conv_state, t0, len, kh, j, *qk_sh ? 0 : 2, 3, tid);
+            }
+            conv_tile(a, sm, min(TC_C, len), pad_qk, warp, lane);
+            tc::fence_async_smem();
+        }
 
         // gates and beta of the chunk being computed are fetched one chunk ahead: GDN and beta
         // by threads < 64, the KDA gate tile by every thread (16 rows of its channel)
@@ -324,7 +511,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             // (The V tile keeps the zeros of the async copy: it is contracted over tokens by
             // the transposing MMA, where a NaN row would reach every column even through an
             // exact zero weight.)
-            if (n < TC_C && a.pad_fill != 0.f) {
+            if (!FRONT && n < TC_C && a.pad_fill != 0.f) {
                 const __nv_bfloat16 pf = __float2bfloat16_rn(a.pad_fill);
                 for (int idx = tid; idx < (TC_C - n) * TC_D; idx += TC_THREADS) {
                     const int r = n + idx / TC_D, c = idx % TC_D;
@@ -605,8 +792,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             tc::fence_async_smem();
             __syncthreads();
             if (!last) {  // K|Q tile is free: next chunk's K, Q (and gates) in flight
-                load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
-                cp_async_commit();
+                if (!FRONT) {
+                    load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+                    cp_async_commit();
+                }
                 fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
                 if (KDA) {
                     const int nn = min(TC_C, len - (ch + 1) * TC_C);
@@ -622,8 +811,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
-            if (!last) {  // V tile consumed by the identity MMA: next chunk's V in flight
-                load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid);
+            if (!last) {  // V tile consumed by the identity MMA: next chunk's V (FRONT: the
+                          // raw rows, into the tf32 K|Q buffer the state MMA has read) in flight
+                if (FRONT) load_raw(a, sm, nullptr, t0, len, (ch + 1) * TC_C, kh, j, tid);
+                else load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid);
                 cp_async_commit();
             }
             {
@@ -731,6 +922,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 if (!KDA) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RUD + t0c), w);
             }
             tc::tmem_wait_st();
+            if (FRONT && !last) cp_async_wait_all();  // next chunk's raw rows
             tc::fence_before_sync();
             __syncthreads();
 
@@ -751,6 +943,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     tc::mma_tf32_ts(tm + COL_S, tm + a5 + kk * 8, bk, id128, 1);
                 }
                 tc::mma_commit(bar_b);
+            }
+            if (FRONT && !last) {  // next chunk's q, k, v tiles while the tensor core works
+                conv_tile(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane);
+                tc::fence_async_smem();
             }
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
@@ -810,7 +1006,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 // Orders the streams by decreasing length (stable) so that the longest units start first,
 // and zeroes the unit counter. One block; B <= 1024 per pass of the rank computation.
 __global__ void order_streams_kernel(const int32_t *cu, int B, int T_each, int32_t *perm,
-                                     int *counter) {
+                                     int *counter, int *conv_readers, int n_readers) {
+    for (int i = threadIdx.x; i < n_readers; i += blockDim.x) conv_readers[i] = 0;
     for (int s = threadIdx.x; s < B; s += blockDim.x) {
         const int ls = cu ? cu[s + 1] - cu[s] : T_each;
         int rank = 0;
@@ -838,8 +1035,14 @@ int sm_count() {
 
 }  // namespace
 
-size_t chunk_tc_workspace_bytes(int B) {
-    return (size_t)((B + 64 + 63) / 64) * 64 * sizeof(int32_t) + 256;
+// Workspace: stream order [B] | conv-state reader counts [B * Hk] | 256 B holding the unit
+// counter (the last 256 bytes).
+static size_t order_bytes(int B) { return (size_t)((B + 64 + 63) / 64) * 64 * sizeof(int32_t); }
+static size_t readers_bytes(int B, int Hk) {
+    return (size_t)(((int64_t)B * Hk + 63) / 64) * 64 * sizeof(int32_t);
+}
+size_t chunk_tc_workspace_bytes(int B, int Hk) {
+    return order_bytes(B) + readers_bytes(B, Hk) + 256;
 }
 
 // ---- Fixed, library-owned scratch for callers that cannot hand the library a workspace.
@@ -881,19 +1084,23 @@ bool chunk_tc_supported(const RecArgs &a) {
 }
 
 cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st) {
-    int32_t *perm = reinterpret_cast<int32_t *>(a.workspace);
-    int *counter = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(a.workspace) +
-                                           chunk_tc_workspace_bytes(a.B) - 256);
-    order_streams_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.T_each, perm, counter);
+    unsigned char *ws = reinterpret_cast<unsigned char *>(a.workspace);
+    int32_t *perm = reinterpret_cast<int32_t *>(ws);
+    int *readers = a.front ? reinterpret_cast<int *>(ws + order_bytes(a.B)) : nullptr;
+    int *counter = reinterpret_cast<int *>(ws + chunk_tc_workspace_bytes(a.B, a.front ? a.Hk : 0) - 256);
+    order_streams_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.T_each, perm, counter, readers,
+                                             a.front ? a.B * a.Hk : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     TcParams P;
     P.a = a;
     P.perm = perm;
     P.counter = counter;
+    P.conv_readers = readers;
     P.num_units = a.B * a.Hv;
     const int grid = min(P.num_units, sm_count());
-    auto kern = a.kda ? chunk_tc_kernel<true> : chunk_tc_kernel<false>;
+    auto kern = a.kda ? (a.front ? chunk_tc_kernel<true, true> : chunk_tc_kernel<true, false>)
+                      : (a.front ? chunk_tc_kernel<false, true> : chunk_tc_kernel<false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
     if (e != cudaSuccess) return e;
     kern<<<grid, TC_THREADS, TC_SMEM, st>>>(P);

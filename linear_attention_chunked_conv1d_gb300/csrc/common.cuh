@@ -80,6 +80,11 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
     return __float2bfloat16_rn(x);
 }
 
+// SiLU(y) = y sigmoid(y) = y / (1 + e^-y), with the fast exponential and reciprocal. The conv
+// kernel and the fused front end of the tensor-core recurrence both use it, so that the two
+// paths give identical bits.
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
+
 // Raises a device status flag (LA_DEV_*). `status` points at the library's per-device word.
 __device__ __forceinline__ void raise_status(int *status, int flag) {
     if (status) atomicOr(status, flag);

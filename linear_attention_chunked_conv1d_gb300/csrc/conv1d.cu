@@ -31,9 +31,6 @@ __device__ __forceinline__ int conv_run_base(const int32_t *cu, int s) {
 // channels). The conv output is rounded to T first, exactly as the separate l2 launch would
 // read it back, and the sum of squares is reduced in the same order as that launch, so the
 // fused and the two-launch paths give identical bits.
-// SiLU(y) = y sigmoid(y) = y / (1 + e^-y), with the fast exponential and reciprocal.
-__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
-
 template <typename T, int K, int HD>
 __global__ void __launch_bounds__(CONV_THREADS, 8)
 conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,

@@ -46,14 +46,25 @@ struct RecArgs {
     void *workspace;
     size_t workspace_bytes;
     int *status;
+    // Fused front end (tensor-core kernel only): q, k and v are not read; each block computes
+    // them per chunk from the pre-conv rows x [tok][cd] (cd = 2 Hk dk + Hv dv, packed
+    // q | k | v heads), the depthwise conv weights [cd][conv_k] (+ optional bias [cd]) and
+    // the carried conv states [conv_k - 1][cd] (one per stream, advanced in place).
+    bool front;
+    const void *x, *conv_w, *conv_bias;
+    const uint64_t *conv_state_ptrs;
+    int64_t x_stride;
+    int conv_k;
+    float l2_eps;
 };
 // CUDA-core chunked kernel (fp32 and bf16 activations, head dims 64 and 128).
 cudaError_t launch_chunk_simt(const RecArgs &a, cudaStream_t st);
 
 // Tensor-core (tcgen05) chunked kernel: bf16 activations, dk = dv = 128. Needs a workspace of
-// chunk_tc_workspace_bytes(B) bytes (stream order + unit counter).
+// chunk_tc_workspace_bytes(B, Hk) bytes (stream order, unit counter and, for the fused front
+// end, one conv-state reader count per (stream, k-head)); Hk = 0 sizes it without the counts.
 bool chunk_tc_supported(const RecArgs &a);
-size_t chunk_tc_workspace_bytes(int B);
+size_t chunk_tc_workspace_bytes(int B, int Hk);
 cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st);
 // Library-owned scratch usable in place of a workspace by the tensor-core kernel (at most
 // chunk_tc_static_scratch_max_streams() streams per call).

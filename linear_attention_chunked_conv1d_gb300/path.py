@@ -6,8 +6,11 @@ prefill_gdn_full_batched when all streams have one length, else the varlen call)
 
     conv1d + SiLU (per stream, carried conv state)  ->  L2 over the q|k heads  ->  recurrence
 
-The packed front-end output [tokens][q heads | k heads | v heads] is handed to the recurrence
-as three strided views (q, k, v), which is all the pages' split_widen step amounts to here.
+With bf16 activations and head dim 128 the whole pass is one launch (`fused`, the library's
+la_prefill_front): the tensor-core recurrence computes its q, k, v tiles from the pre-conv rows
+itself. Otherwise (and in `run_unfused`) the packed front-end output
+[tokens][q heads | k heads | v heads] is handed to the recurrence as three strided views
+(q, k, v), which is all the pages' split_widen step amounts to here.
 This module only sequences the library calls; it holds no arithmetic.
 """
 from __future__ import annotations
@@ -17,9 +20,8 @@ import math
 import torch
 
 from . import (conv1d_silu_l2_prefill, conv1d_silu_prefill, conv1d_silu_prefill_varlen,
-               gdn_prefill_batched,
-               gdn_prefill_varlen, kda_prefill, l2norm_heads, pointer_array,
-               prefill_workspace_bytes)
+               gdn_prefill_batched, gdn_prefill_varlen, kda_prefill, l2norm_heads,
+               pointer_array, prefill_front, prefill_workspace_bytes)
 
 
 class PrefillPass:
@@ -51,6 +53,7 @@ class PrefillPass:
         self.k = self.conv_out[:, hk:2 * hk]
         self.v = self.conv_out[:, 2 * hk:]
         self.scale = 1.0 / math.sqrt(wl.d)
+        self.can_fuse = x.dtype == torch.bfloat16 and wl.d == 128
 
     def front_end(self, stream=None):
         """conv1d + SiLU and the q|k L2 norm in one fused launch (bitwise equal to the two)."""
@@ -86,7 +89,22 @@ class PrefillPass:
             gdn_prefill_varlen(self.h_ptrs, self.q, self.k, self.v, inp["g"], inp["beta"],
                                self.out, inp["cu_seqlens"], max_seqlen=self.max_seqlen, **common)
 
-    def run(self, stream=None):
+    def fused(self, stream=None):
+        """conv1d + SiLU + L2 + recurrence in one launch (bf16, head dim 128)."""
+        wl, inp = self.wl, self.inp
+        prefill_front(self.conv_state_ptrs, self.h_ptrs, inp["x"], inp["conv_w"], inp["g"],
+                      inp["beta"], self.out, None if wl.batched or wl.B == 1 else inp["cu_seqlens"],
+                      B=wl.B, Hk=wl.Hk, Hv=wl.Hv, dk=wl.d, dv=wl.d, kda=wl.variant == "kda",
+                      max_seqlen=self.max_seqlen, l2_eps=self.eps, scale=self.scale,
+                      pad_fill=self.pad_fill, workspace=self.workspace, stream=stream)
+
+    def run_unfused(self, stream=None):
         self.front_end(stream)
         self.recurrence(stream)
         return self.out
+
+    def run(self, stream=None):
+        if self.can_fuse:
+            self.fused(stream)
+            return self.out
+        return self.run_unfused(stream)

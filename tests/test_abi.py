@@ -133,3 +133,43 @@ def test_binding_raises_typed_error(lib):
 
 def test_workspace_query(lib):
     assert lib.prefill_workspace_bytes(4, 1000, 16, 32, 128, 128, lib.LA_BF16) >= 0
+
+
+def _rc_front(lib, **kw):
+    """la_prefill_front with fake addresses; every case here is refused before any launch."""
+    a = dict(cs=A, hs=A, x=A, w=A, bias=None, K=4, g=A, beta=A, out=A * 2, cu=A, B=2, total=40,
+             max_seqlen=30, max_tokens=100, Hk=1, Hv=2, dk=128, dv=128, xs=512, eps=1e-6,
+             scale=0.1, pad=0.0, kda=0, dtype=1, ws=A * 3, wsb=1 << 20)
+    a.update(kw)
+    return lib._load().la_prefill_front(
+        a["cs"], a["hs"], a["x"], a["w"], a["bias"], a["K"], a["g"], a["beta"], a["out"],
+        a["cu"], a["B"], a["total"], a["max_seqlen"], a["max_tokens"], a["Hk"], a["Hv"], a["dk"],
+        a["dv"], a["xs"], a["eps"], a["scale"], a["pad"], a["kda"], a["dtype"], a["ws"],
+        a["wsb"], 0)
+
+
+def test_fused_prefill_refusals(lib):
+    assert _rc_front(lib, total=0) == lib.LA_ERR_COUNT
+    assert _rc_front(lib, total=101) == lib.LA_ERR_COUNT
+    assert _rc_front(lib, dtype=0) == lib.LA_ERR_UNSUPPORTED          # fp32: separate calls
+    assert _rc_front(lib, dk=64, dv=64) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_front(lib, K=5) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_front(lib, kda=2) == lib.LA_ERR_ARG
+    assert _rc_front(lib, Hv=3, Hk=2) == lib.LA_ERR_ARG               # Hv % Hk
+    assert _rc_front(lib, cu=None, total=41) == lib.LA_ERR_ARG        # batched: 41 % 2
+    assert _rc_front(lib, max_seqlen=41) == lib.LA_ERR_ARG
+    assert _rc_front(lib, cs=None) == lib.LA_ERR_ARG                  # conv state needed (K > 1)
+    assert _rc_front(lib, x=A + 4) == lib.LA_ERR_ARG                  # misaligned
+    assert _rc_front(lib, xs=500) == lib.LA_ERR_ARG                   # stride < 2 Hk dk + Hv dv
+    assert _rc_front(lib, out=A) == lib.LA_ERR_ARG                    # aliases x
+    assert _rc_front(lib, eps=-1.0) == lib.LA_ERR_ARG
+    assert _rc_front(lib, wsb=16) == lib.LA_ERR_ARG                   # workspace too small
+    assert _rc_front(lib, ws=None) == lib.LA_ERR_ARG
+    assert "workspace" in lib.last_error()
+
+
+def test_workspace_grows_with_conv_reader_counts(lib):
+    L = lib._load()
+    small = L.la_prefill_workspace_bytes(4, 100, 1, 4, 128, 128, 1)
+    big = L.la_prefill_workspace_bytes(4, 100, 64, 64, 128, 128, 1)
+    assert big > small and big % 16 == 0 and small % 16 == 0
