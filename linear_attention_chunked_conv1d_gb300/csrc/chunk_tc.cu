@@ -83,8 +83,8 @@ constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 
                    SF_WARP = 704 + 128 * NQ, SF_RF = SF_WARP + 8, SF_CF = SF_RF + 64,
                    SF_END = SF_CF + 64;
 constexpr uint32_t SM_BARS = SM_SMALL + SF_END * 4;  // mbarriers, flags, tmem base (64 B)
-// fused front end: conv taps (fp32 [3 x 128 channels][4], leading taps zero when kernel < 4)
-// and bias of the unit's q | k | v channels; the raw rows share the tf32 K|Q buffer
+// fused front end: conv taps (fp32 [4 taps][3 x 128 channels], leading taps zero when
+// kernel < 4) and bias of the unit's q | k | v channels; the raw rows share the tf32 K|Q buffer
 constexpr uint32_t SM_CW = SM_BARS + 64;
 constexpr uint32_t SM_CB = SM_CW + 3 * TC_D * 16;
 constexpr uint32_t SM_RAW = SM_KQG;             // bf16 [67 rows][384 channels]
@@ -175,19 +175,19 @@ __device__ __forceinline__ int front_channel(const RecArgs &a, int sec, int kh, 
     return sec == 0 ? kh * TC_D : sec == 1 ? (a.Hk + kh) * TC_D : (2 * a.Hk + j) * TC_D;
 }
 
-// Conv taps and bias of the unit's 384 channels -> shared memory (fp32, taps right-aligned).
+// Conv taps and bias of the unit's 384 channels -> shared memory (fp32, tap-major, taps
+// right-aligned: tap m of a kernel-K conv sits at row m + 4 - K).
 __device__ __forceinline__ void load_conv_weights(const RecArgs &a, unsigned char *sm, int kh,
                                                   int j, int tid) {
     const __nv_bfloat16 *w = reinterpret_cast<const __nv_bfloat16 *>(a.conv_w);
     const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(a.conv_bias);
     const int K = a.conv_k;
+    float *cw = reinterpret_cast<float *>(sm + SM_CW);
     for (int idx = tid; idx < 3 * TC_D; idx += TC_THREADS) {
         const int ch = front_channel(a, idx / TC_D, kh, j) + idx % TC_D;
-        float tap[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-            tap[m] = m >= 4 - K ? __bfloat162float(w[(int64_t)ch * K + m - (4 - K)]) : 0.f;
-        reinterpret_cast<float4 *>(sm + SM_CW)[idx] = make_float4(tap[0], tap[1], tap[2], tap[3]);
+            cw[m * 3 * TC_D + idx] = m >= 4 - K ? __bfloat162float(w[(int64_t)ch * K + m - (4 - K)]) : 0.f;
         reinterpret_cast<float *>(sm + SM_CB)[idx] = b ? __bfloat162float(b[ch]) : 0.f;
     }
 }
@@ -201,82 +201,124 @@ __device__ __forceinline__ void load_raw(const RecArgs &a, unsigned char *sm,
     const __nv_bfloat16 *x = reinterpret_cast<const __nv_bfloat16 *>(a.x);
     const int64_t cd = (int64_t)(2 * a.Hk + a.Hv) * TC_D;
     const int K1 = a.conv_k - 1;
-    const uint32_t base = tc::smem_u32(sm + SM_RAW);
-    for (int idx = tid; idx < RAW_ROWS * 48; idx += TC_THREADS) {
-        const int rho = idx / 48, cc = idx - rho * 48;  // cc: 16-byte piece, 16 per section
-        const int ch = front_channel(a, cc >> 4, kh, j) + (cc & 15) * 8;
-        const int r = rel0 - 3 + rho;
-        const __nv_bfloat16 *src = x;
-        bool valid;
-        if (r >= 0) {
-            valid = r < len;
-            if (valid) src = x + (int64_t)(t0 + r) * a.x_stride + ch;
-        } else {
-            valid = state != nullptr && K1 + r >= 0;
-            if (valid) src = state + (int64_t)(K1 + r) * cd + ch;
+    // thread t < 480 copies 16-byte piece t % 48 (16 per section) of raw rows t / 48 + 10 m
+    if (tid >= 480) return;
+    const int cc = tid % 48, rho0 = tid / 48;
+    const int ch = front_channel(a, cc >> 4, kh, j) + (cc & 15) * 8;
+    const uint32_t dst = tc::smem_u32(sm + SM_RAW) + rho0 * RAW_LD + cc * 16;
+    const int64_t xs = a.x_stride;
+#pragma unroll
+    for (int m = 0; m < 7; ++m) {
+        const int rho = rho0 + 10 * m;
+        if (rho < RAW_ROWS) {
+            const int r = rel0 - 3 + rho;
+            const __nv_bfloat16 *src = x;
+            bool valid;
+            if (r >= 0) {
+                valid = r < len;
+                if (valid) src = x + (int64_t)(t0 + r) * xs + ch;
+            } else {
+                valid = state != nullptr && K1 + r >= 0;
+                if (valid) src = state + (int64_t)(K1 + r) * cd + ch;
+            }
+            cp_async16(dst + 10 * m * RAW_LD, src, valid);
         }
-        cp_async16(base + rho * RAW_LD + cc * 16, src, valid);
     }
+}
+
+// Packed pairs of fp32 (Blackwell f32x2 ALU ops; each lane rounds like the scalar op).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16 pair (low half = first element) widened to an fp32 pair
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+    return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 // q, k, v tiles of a chunk from its raw rows: out[t][c] = SiLU(b[c] + sum_m w[c][m] xh[t-3+m][c])
 // rounded to bf16, then q and k rows scaled by 1/sqrt(sum of squares + eps) and rounded again.
 // Warp w takes rows 4w..4w+3, lane l the channel quad 4l..4l+3 of each section: a section row
 // is one warp, reduced with xor-shuffles in the order of the L2 kernel. Rows >= n get pad (q, k)
-// or zero (v).
+// or zero (v). K4: a 4-tap conv (no leading zero taps to skip).
+template <bool K4>
 __device__ __forceinline__ void conv_tile(const RecArgs &a, unsigned char *sm, int n, float pad,
                                           int warp, int lane) {
-    const float4 *cw = reinterpret_cast<const float4 *>(sm + SM_CW);
+    const float *cw = reinterpret_cast<const float *>(sm + SM_CW);
     const float *cb = reinterpret_cast<const float *>(sm + SM_CB);
-    const int K = a.conv_k;
+    const int m0 = K4 ? 0 : 4 - a.conv_k;  // first tap that is not zero
     const int tau0 = 4 * warp;
     const __nv_bfloat162 pf2 = __float2bfloat162_rn(pad);
     const uint32_t pfw = *reinterpret_cast<const uint32_t *>(&pf2);
 #pragma unroll 1
     for (int sec = 0; sec < 3; ++sec) {
         const int c0 = sec * TC_D + 4 * lane;
-        float wt[4][4], bs[4];
+        uint64_t w01[4], w23[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 wv = cw[c0 + e];
-            wt[e][0] = wv.x; wt[e][1] = wv.y; wt[e][2] = wv.z; wt[e][3] = wv.w;
-            bs[e] = cb[c0 + e];
+        for (int m = 0; m < 4; ++m) {
+            const float4 wv = *reinterpret_cast<const float4 *>(cw + m * 3 * TC_D + c0);
+            w01[m] = pk2(wv.x, wv.y);
+            w23[m] = pk2(wv.z, wv.w);
         }
-        float xr[7][4];
+        const float4 bv = *reinterpret_cast<const float4 *>(cb + c0);
+        uint64_t x01[7], x23[7];
 #pragma unroll
         for (int i = 0; i < 7; ++i) {
             const uint2 raw = *reinterpret_cast<const uint2 *>(sm + SM_RAW + (tau0 + i) * RAW_LD + c0 * 2);
-            xr[i][0] = __uint_as_float(raw.x << 16);
-            xr[i][1] = __uint_as_float(raw.x & 0xFFFF0000u);
-            xr[i][2] = __uint_as_float(raw.y << 16);
-            xr[i][3] = __uint_as_float(raw.y & 0xFFFF0000u);
+            x01[i] = bf2_to_f2(raw.x);
+            x23[i] = bf2_to_f2(raw.y);
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int tau = tau0 + q;
-            float y[4];
+            uint64_t a01 = pk2(bv.x, bv.y), a23 = pk2(bv.z, bv.w);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float acc = bs[e];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) acc = fmaf(wt[e][m], m >= 4 - K ? xr[q + m][e] : 0.f, acc);
-                y[e] = silu(acc);
+            for (int m = 0; m < 4; ++m) {
+                if (K4 || m >= m0) {
+                    a01 = fma2(w01[m], x01[q + m], a01);
+                    a23 = fma2(w23[m], x23[q + m], a23);
+                }
             }
+            float y[4];
+            upk2(a01, y[0], y[1]);
+            upk2(a23, y[2], y[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[e] = silu(y[e]);
+            __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
             if (sec < 2) {
+                // the conv output as stored (bf16), then the L2 of the row
+                uint32_t wl = *reinterpret_cast<const uint32_t *>(&lo);
+                uint32_t wh = *reinterpret_cast<const uint32_t *>(&hi);
+                const uint64_t r01 = bf2_to_f2(wl), r23 = bf2_to_f2(wh);
+                upk2(r01, y[0], y[1]);
+                upk2(r23, y[2], y[3]);
                 float ss = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    y[e] = __bfloat162float(__float2bfloat16_rn(y[e]));
-                    ss = fmaf(y[e], y[e], ss);
-                }
+                for (int e = 0; e < 4; ++e) ss = fmaf(y[e], y[e], ss);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
                 const float inv = rsqrtf(ss + a.l2_eps);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) y[e] *= inv;
+                const uint64_t iv = pk2(inv, inv);
+                upk2(mul2(r01, iv), y[0], y[1]);
+                upk2(mul2(r23, iv), y[2], y[3]);
+                lo = __floats2bfloat162_rn(y[0], y[1]);
+                hi = __floats2bfloat162_rn(y[2], y[3]);
             }
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
             uint2 packed = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
                                       *reinterpret_cast<const uint32_t *>(&hi));
             if (tau >= n) packed = sec < 2 ? make_uint2(pfw, pfw) : make_uint2(0u, 0u);
@@ -285,6 +327,11 @@ __device__ __forceinline__ void conv_tile(const RecArgs &a, unsigned char *sm, i
             *reinterpret_cast<uint2 *>(sm + off) = packed;
         }
     }
+}
+__device__ __forceinline__ void conv_tile_any(const RecArgs &a, unsigned char *sm, int n,
+                                              float pad, int warp, int lane) {
+    if (a.conv_k == 4) conv_tile<true>(a, sm, n, pad, warp, lane);
+    else conv_tile<false>(a, sm, n, pad, warp, lane);
 }
 
 // New conv state of a stream, rows i < kernel - 1 = stream rows len - (kernel - 1) + i of
@@ -431,7 +478,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 __syncthreads();
                 write_conv_state(a, sm, conv_state, t0, len, kh, j, *qk_sh ? 0 : 2, 3, tid);
             }
-            conv_tile(a, sm, min(TC_C, len), pad_qk, warp, lane);
+            conv_tile_any(a, sm, min(TC_C, len), pad_qk, warp, lane);
             tc::fence_async_smem();
         }
 
@@ -945,7 +992,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 tc::mma_commit(bar_b);
             }
             if (FRONT && !last) {  // next chunk's q, k, v tiles while the tensor core works
-                conv_tile(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane);
+                conv_tile_any(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane);
                 tc::fence_async_smem();
             }
             wait_bar(bar_b, phase_b);
