@@ -31,10 +31,13 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from linear_attention_chunked_conv1d_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+from linear_attention_chunked_conv1d_gb300.inputs import (  # noqa: E402
+    DECODE_WORKLOADS, WORKLOADS, make_inputs)
 
 DEFAULT_WORKLOAD = "gdn_batched_8x2048_h16_d128"
 METRIC = "prefill tokens/s per GDN/KDA layer"
+DECODE_METRIC = "decode tokens/s per GDN/KDA layer"
+ALL_WORKLOADS = {**WORKLOADS, **DECODE_WORKLOADS}
 CHUNK = 64
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -58,6 +61,17 @@ def path_algorithmic(wl, lengths):
     B = per_tok * T + per_stream * len(lengths) + wl.cd * K * s
     F = T * wl.Hv * (2 * CHUNK * d + CHUNK * 2 * d + CHUNK * d + 6 * d * d)
     return B, F
+
+
+def decode_algorithmic_bytes(wl):
+    """Algorithmic bytes of one decode step (B streams, one token each): x row, gates, output,
+    h state read + written, conv state read + written, per stream; conv weights once."""
+    s = act_bytes(wl)
+    d, K = wl.d, wl.conv_kernel
+    gate = 4 * wl.Hv * (d if wl.variant == "kda" else 1)
+    per_stream = (wl.cd * s + gate + 4 * wl.Hv + wl.Hv * d * s + 2 * 4 * wl.Hv * d * d
+                  + 2 * s * (K - 1) * wl.cd)
+    return per_stream * wl.B + wl.cd * K * s
 
 
 def kernel_algorithmic_bytes(wl, lengths):
@@ -229,7 +243,8 @@ def run_reference(args, wl):
     total = sum(times)
     value = toks / total
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": DECODE_METRIC if wl.mode == "decode" else METRIC,
+        "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe in DESIGN.md)",
@@ -269,12 +284,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(ALL_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    wl = WORKLOADS[args.workload]
+    wl = ALL_WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
         return
@@ -295,6 +310,9 @@ def main():
 
     la._load()
     inp = make_inputs(wl, device=dev, seed=rank)  # each replica its own batch (weak scaling)
+    if wl.mode == "decode":
+        run_decode(args, wl, inp, dev, local, rank, world, pg)
+        return
     lengths = inp["lengths"]
     T = sum(lengths)
     p = PrefillPass(wl, inp)
@@ -439,6 +457,102 @@ def main():
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms * 1e-3),
                           "bytes_alg": B_alg, "flops_alg": F_alg,
                           "peaks": f"{peak_src}: {hbm} GB/s, {peaks['bf16_tflops']} TFLOP/s bf16"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def run_decode(args, wl, inp, dev, local, rank, world, pg):
+    """One step = one decode step of the layer for B streams (one new token each), states in
+    HBM: la_decode_step (conv + SiLU + L2 launch, then the recurrence launch)."""
+    from linear_attention_chunked_conv1d_gb300.path import DecodeStep
+
+    p = DecodeStep(wl, inp)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        p.run()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        p.run()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    T = wl.B
+    value, ms, _ = aggregate(T, sum(step_ms) / len(step_ms), pg, dev)
+
+    # end to end through the public API: this step's token rows, gates in; outputs out
+    x_h = inp["x"].cpu().pin_memory()
+    g_h = inp["g"].cpu().pin_memory()
+    b_h = inp["beta"].cpu().pin_memory()
+    out_h = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (x_h, g_h, b_h))
+    d2h = out_h.numel() * out_h.element_size()
+    for _ in range(2):
+        inp["x"].copy_(x_h, non_blocking=True)
+        p.run()
+        out_h.copy_(p.out, non_blocking=True)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        inp["x"].copy_(x_h, non_blocking=True)
+        inp["g"].copy_(g_h, non_blocking=True)
+        inp["beta"].copy_(b_h, non_blocking=True)
+        p.run()
+        out_h.copy_(p.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _, _ = aggregate(T, e0.elapsed_time(e1) / args.steps, pg, dev)
+    if rank != 0:
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    step_avg = sum(step_ms) / len(step_ms)
+    B_alg = decode_algorithmic_bytes(wl)
+    achieved = B_alg / (step_avg * 1e-3) / 1e9
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded; x~N(0,1), conv w~N(0,0.25), conv state~N(0,1), "
+                "h~N(0,0.02), g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
+        "config": {"workload": wl.name, "streams": wl.B, "tokens_per_step": T, "Hk": wl.Hk,
+                   "Hv": wl.Hv, "head_dim": wl.d, "variant": wl.variant,
+                   "activations": wl.dtype, "states": "f32",
+                   "path": "la_decode_step (conv1d+SiLU+L2 launch, recurrence launch)",
+                   "compute": "CUDA cores fp32 (matrix-vector work per state)",
+                   "l2": "flushed between timed steps (write of a 258 MiB buffer); the h states "
+                         f"({wl.B * wl.Hv * wl.d * wl.d * 4 >> 20} MiB) exceed L2 as well",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode step (conv1d_silu_kernel + decode_rec_kernel; the events "
+                               "bracket both launches)",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": B_alg, "avg_launch_ms": step_avg},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)

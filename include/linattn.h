@@ -242,6 +242,30 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
                      int kda, int dtype, void *workspace, size_t workspace_bytes,
                      uint64_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Decode step: one new token for each of B streams, on the carried conv and h states (the step
+ * that follows a prefill). "glm5next_kda/prefill.rs", Glm5NextKdaLayer::prefill_with_pad_fill:
+ * the layer's decode_k shares the prefill's front-end and recurrence buckets, i.e. it is the same
+ * layer applied to one token per stream: conv1d + SiLU over the conv state (which shifts by one
+ * row), L2 of each q and k head, then one step of the recurrence on H = S^T.
+ *
+ * x             [B][x_stride] (dtype): row s is stream s's new token, cd = 2*Hk*dk + Hv*dv
+ *               channels packed [q heads | k heads | v heads].
+ * conv_state_ptrs, h_state_ptrs  as for la_prefill_front (one conv and one h state per stream,
+ *               updated in place); each h state 16-byte aligned.
+ * conv_w, conv_bias, conv_kernel, l2_eps, scale  as for la_prefill_front.
+ * g, beta       GDN (kda == 0): g [B][Hv]; KDA (kda == 1): g [B][Hv][dk]; beta [B][Hv]; fp32.
+ * out           [B][Hv][dv] (dtype, contiguous).
+ * workspace     at least la_decode_workspace_bytes(...) bytes (holds the conv output).
+ * dtype LA_F32 or LA_BF16; dk = dv in {64, 128}; conv_kernel 1..4. Two launches (front end,
+ * recurrence), CUDA cores, fp32 arithmetic. Count rule: 1 <= B <= max_streams. */
+size_t la_decode_workspace_bytes(int B, int Hk, int Hv, int dk, int dv, int dtype);
+int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs,
+                   const void *x, const void *conv_w, const void *conv_bias, int conv_kernel,
+                   const float *g, const float *beta, void *out, int B, int max_streams, int Hk,
+                   int Hv, int dk, int dv, int64_t x_stride, float l2_eps, float scale, int kda,
+                   int dtype, void *workspace, size_t workspace_bytes, uint64_t stream);
+
 #ifdef __cplusplus
 }
 #endif

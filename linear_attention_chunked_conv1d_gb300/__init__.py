@@ -70,6 +70,9 @@ _SIGS = {
     "la_prefill_front": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                           _i32, _i32, _i32, _i32, _i32, _i64, _f32, _f32, _f32, _i32, _i32, _vp,
                           _sz, _u64], ctypes.c_int),
+    "la_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
+    "la_decode_step": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                        _i32, _i32, _i64, _f32, _f32, _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
 }
 
 _lib = None
@@ -276,3 +279,24 @@ def prefill_front(conv_state_ptrs, h_state_ptrs, x, conv_w, gate, beta, out, cu_
         max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(x),
         float(l2_eps), float(scale), float(pad_fill), 1 if kda else 0, _dtype_code(x),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def decode_workspace_bytes(B, Hk, Hv, dk, dv, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (LA_BF16 if dtype == torch.bfloat16 else LA_F32)
+    return int(_load().la_decode_workspace_bytes(B, Hk, Hv, dk, dv, code))
+
+
+def decode_step(conv_state_ptrs, h_state_ptrs, x, conv_w, gate, beta, out, *, Hk, Hv, dk, dv,
+                kda, conv_bias=None, l2_eps=1e-6, scale=None, max_streams=None, workspace=None,
+                stream=None) -> None:
+    """One decode step: x [B][cd] holds one new token per stream; conv and h states advance
+    in place; out [B][Hv][dv]."""
+    B = x.shape[0]
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _, K = conv_w.shape
+    _check(_load().la_decode_step(
+        _ptr(conv_state_ptrs), _ptr(h_state_ptrs), _ptr(x), _ptr(conv_w), _ptr(conv_bias), K,
+        _ptr(gate), _ptr(beta), _ptr(out), B, max_streams if max_streams is not None else B, Hk,
+        Hv, dk, dv, _row_stride(x), float(l2_eps), float(scale), 1 if kda else 0,
+        _dtype_code(x), _ptr(workspace), ws_bytes, _stream(stream)))

@@ -429,4 +429,66 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
     return launch_result(la::launch_chunk_tc(a, as_stream(stream)), "fused prefill (tcgen05) launch");
 }
 
+size_t la_decode_workspace_bytes(int B, int Hk, int Hv, int dk, int dv, int dtype) {
+    if (B < 1 || Hk < 1 || Hv < 1 || dk < 1 || dv < 1) return 0;
+    const size_t cd = (size_t)(2 * Hk) * dk + (size_t)Hv * dv;
+    const size_t row = (cd * (dtype == LA_BF16 ? 2 : 4) + 15) / 16 * 16;
+    return (size_t)B * row;
+}
+
+int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs,
+                   const void *x, const void *conv_w, const void *conv_bias, int conv_kernel,
+                   const float *g, const float *beta, void *out, int B, int max_streams, int Hk,
+                   int Hv, int dk, int dv, int64_t x_stride, float l2_eps, float scale, int kda,
+                   int dtype, void *workspace, size_t workspace_bytes, uint64_t stream) {
+    if (B < 1 || B > max_streams)
+        return fail(LA_ERR_COUNT, "decode step of %d streams does not fit max_streams %d", B,
+                    max_streams);
+    LA_TRY(check_dtype(dtype));
+    if (kda != 0 && kda != 1) return fail(LA_ERR_ARG, "kda must be 0 (GDN) or 1 (KDA)");
+    if (Hk < 1 || Hv < 1) return fail(LA_ERR_ARG, "Hk and Hv must be >= 1 (got %d, %d)", Hk, Hv);
+    if (Hv % Hk) return fail(LA_ERR_ARG, "Hv (%d) is not a multiple of Hk (%d)", Hv, Hk);
+    if ((dk != 64 && dk != 128) || dv != dk)
+        return fail(LA_ERR_UNSUPPORTED, "head dims dk=%d dv=%d: compiled for dk = dv in {64, 128}",
+                    dk, dv);
+    if (conv_kernel < 1 || conv_kernel > 4)
+        return fail(LA_ERR_UNSUPPORTED, "conv kernel %d outside the compiled 1..4", conv_kernel);
+    const int64_t cd = (int64_t)(2 * Hk) * dk + (int64_t)Hv * dv;
+    if (!h_state_ptrs) return fail(LA_ERR_ARG, "h_state_ptrs is NULL");
+    if (conv_kernel > 1 && !conv_state_ptrs) return fail(LA_ERR_ARG, "conv_state_ptrs is NULL");
+    LA_TRY(check_act_ptr(x, "x"));
+    LA_TRY(check_act_ptr(out, "out"));
+    LA_TRY(check_act_ptr(conv_bias, "conv_bias", true));
+    if (!conv_w) return fail(LA_ERR_ARG, "conv_w is NULL");
+    if (!g) return fail(LA_ERR_ARG, "g is NULL");
+    if (!beta) return fail(LA_ERR_ARG, "beta is NULL");
+    LA_TRY(check_stride(x_stride, cd, dtype, "x_stride"));
+    if (x == out) return fail(LA_ERR_ARG, "out may not alias x");
+    if (!(l2_eps >= 0.f)) return fail(LA_ERR_ARG, "l2_eps must be >= 0");
+    const size_t need = la_decode_workspace_bytes(B, Hk, Hv, dk, dv, dtype);
+    if (workspace_bytes < need)
+        return fail(LA_ERR_ARG, "workspace of %zu bytes is below the %zu required", workspace_bytes,
+                    need);
+    if (!workspace || !aligned16(workspace))
+        return fail(LA_ERR_ARG, "workspace is NULL or not 16-byte aligned");
+    const int64_t row = (int64_t)(need / (size_t)B) / (dtype == LA_BF16 ? 2 : 4);  // elements
+    int *status = status_ptr();
+    la::ConvArgs c{};
+    c.state_ptrs = conv_state_ptrs;
+    c.x = x; c.w = conv_w; c.bias = conv_bias; c.out = workspace;
+    c.cu = nullptr; c.B = B; c.total = B; c.channels = (int)cd; c.kernel = conv_kernel;
+    c.x_stride = x_stride; c.out_stride = row; c.dtype = dtype;
+    c.l2_heads = 2 * Hk; c.head_dim = dk; c.eps = l2_eps;
+    c.status = status;
+    c.one_per_stream = true;
+    cudaStream_t st = as_stream(stream);
+    cudaError_t e = la::launch_conv1d_silu(c, st);
+    if (e != cudaSuccess) return launch_result(e, "decode front end launch");
+    la::DecArgs d{};
+    d.h_ptrs = h_state_ptrs; d.qkv = workspace; d.qkv_stride = row;
+    d.g = g; d.beta = beta; d.out = out;
+    d.B = B; d.Hk = Hk; d.Hv = Hv; d.d = dk; d.scale = scale; d.dtype = dtype; d.kda = kda == 1;
+    return launch_result(la::launch_decode_recurrence(d, st), "decode recurrence launch");
+}
+
 }  // extern "C"

@@ -37,7 +37,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                    const T *__restrict__ x, const T *__restrict__ w,
                    const T *__restrict__ bias, T *__restrict__ out,
                    const int32_t *__restrict__ cu, int B, int total, int C, int64_t xs,
-                   int64_t os, int n_l2, float eps, int *status) {
+                   int64_t os, int n_l2, float eps, int *status, bool one_per_stream) {
     using V = Vec4<T>;
     constexpr int N = V::N;
     constexpr int LPH = HD > 0 ? HD / N : 1;  // lanes per head
@@ -48,7 +48,12 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 
     // Which stream and which run of it this block covers.
     int s = 0, sb = 0, se = total, run = blockIdx.x;
-    if (cu) {
+    if (one_per_stream) {  // decode: row s is the one token of stream s
+        s = blockIdx.x;
+        sb = s;
+        se = s + 1;
+        run = 0;
+    } else if (cu) {
         if (cu[0] != 0 || cu[B] != total) {
             if (threadIdx.x == 0) raise_status(status, LA_DEV_BAD_SEQLENS);
             return;
@@ -183,12 +188,13 @@ static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
     int nvec = a.channels / N;
     // Run slots: single stream ceil(total/ROWS); varlen floor(total/ROWS) + B covers every
     // stream's runs (stream s starts at slot floor(cu[s]/ROWS) + s).
-    int slots = a.cu ? a.total / CONV_ROWS + a.B : (a.total + CONV_ROWS - 1) / CONV_ROWS;
+    int slots = a.one_per_stream ? a.B
+                : a.cu ? a.total / CONV_ROWS + a.B : (a.total + CONV_ROWS - 1) / CONV_ROWS;
     dim3 grid(slots, (nvec + CONV_THREADS - 1) / CONV_THREADS);
     conv1d_silu_kernel<T, K, HD><<<grid, CONV_THREADS, 0, st>>>(
         a.state_ptrs, (T *)a.single_state, (const T *)a.x, (const T *)a.w, (const T *)a.bias,
         (T *)a.out, a.cu, a.B, a.total, a.channels, a.x_stride, a.out_stride,
-        a.l2_heads * a.head_dim, a.eps, a.status);
+        a.l2_heads * a.head_dim, a.eps, a.status, a.one_per_stream);
     return cudaGetLastError();
 }
 

@@ -18,6 +18,7 @@ struct ConvArgs {
     int l2_heads, head_dim;  // l2_heads > 0: fused L2 over the first l2_heads * head_dim channels
     float eps;
     int *status;
+    bool one_per_stream;  // decode: B streams of one token, token s = row s (cu unused)
 };
 cudaError_t launch_conv1d_silu(const ConvArgs &a, cudaStream_t st);
 
@@ -70,5 +71,20 @@ cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st);
 // chunk_tc_static_scratch_max_streams() streams per call).
 int chunk_tc_static_scratch_max_streams();
 cudaError_t chunk_tc_static_scratch(void **ptr, size_t *bytes);
+
+// Decode step of the recurrence: one token per stream, q|k|v rows [B][qkv_stride] (the conv
+// output), states through h_ptrs, out [B][Hv][dv]. CUDA cores, fp32 arithmetic.
+struct DecArgs {
+    const uint64_t *h_ptrs;
+    const void *qkv;
+    int64_t qkv_stride;
+    const float *g, *beta;  // GDN g [B][Hv]; KDA g [B][Hv][dk]; beta [B][Hv]
+    void *out;
+    int B, Hk, Hv, d;
+    float scale;
+    int dtype;
+    bool kda;
+};
+cudaError_t launch_decode_recurrence(const DecArgs &a, cudaStream_t st);
 
 }  // namespace la

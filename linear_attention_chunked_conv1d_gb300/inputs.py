@@ -35,6 +35,7 @@ class Workload:
     x_std: float = 1.0
     w_std: float = 0.25
     batched: bool = False      # equal-length streams through the batched call
+    mode: str = "prefill"      # "prefill", or "decode": one new token per stream (lengths fixed:1)
 
     @property
     def cd(self) -> int:
@@ -67,6 +68,18 @@ WORKLOADS = {
     "kda_varlen_64_h32_d128": Workload("kda_varlen_64_h32_d128", "kda", 64, 32, 32, 128,
                                        "loguniform:16:16384:262144", conv_state="randn",
                                        h_state="randn"),
+}
+
+# Decode steps (one token for each of 256 streams, carried states), the step after a prefill.
+DECODE_WORKLOADS = {
+    # GDN, 16 q/k heads shared by 32 v heads, d = 128, as the GDN varlen prefill
+    "gdn_decode_256_hk16_hv32_d128": Workload("gdn_decode_256_hk16_hv32_d128", "gdn", 256, 16, 32,
+                                              128, "fixed:1", conv_state="randn",
+                                              h_state="randn", mode="decode"),
+    # KDA, 32 heads, d = 128, as the KDA prefills
+    "kda_decode_256_h32_d128": Workload("kda_decode_256_h32_d128", "kda", 256, 32, 32, 128,
+                                        "fixed:1", conv_state="randn", h_state="randn",
+                                        mode="decode"),
 }
 
 

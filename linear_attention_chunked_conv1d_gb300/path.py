@@ -20,8 +20,8 @@ import math
 import torch
 
 from . import (conv1d_silu_l2_prefill, conv1d_silu_prefill, conv1d_silu_prefill_varlen,
-               gdn_prefill_batched, gdn_prefill_varlen, kda_prefill, l2norm_heads,
-               pointer_array, prefill_front, prefill_workspace_bytes)
+               decode_step, decode_workspace_bytes, gdn_prefill_batched, gdn_prefill_varlen,
+               kda_prefill, l2norm_heads, pointer_array, prefill_front, prefill_workspace_bytes)
 
 
 class PrefillPass:
@@ -108,3 +108,31 @@ class PrefillPass:
             self.fused(stream)
             return self.out
         return self.run_unfused(stream)
+
+
+class DecodeStep:
+    """One decode step of a GDN/KDA layer for B streams (one new token each) on one device,
+    through la_decode_step. `inputs` as for PrefillPass, with x [B][cd] (row s = stream s)."""
+
+    def __init__(self, wl, inputs: dict, *, eps: float = 1e-6):
+        self.wl = wl
+        self.inp = inputs
+        self.eps = eps
+        x = inputs["x"]
+        B = wl.B
+        assert x.shape[0] == B, "a decode step takes one token per stream"
+        dev = x.device
+        self.out = torch.empty(B, wl.Hv, wl.d, dtype=x.dtype, device=dev)
+        self.conv_state_ptrs = pointer_array([inputs["conv_state"][s] for s in range(B)])
+        self.h_ptrs = pointer_array([inputs["h"][s] for s in range(B)])
+        nbytes = decode_workspace_bytes(B, wl.Hk, wl.Hv, wl.d, wl.d, x.dtype)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.scale = 1.0 / math.sqrt(wl.d)
+
+    def run(self, stream=None):
+        wl, inp = self.wl, self.inp
+        decode_step(self.conv_state_ptrs, self.h_ptrs, inp["x"], inp["conv_w"], inp["g"],
+                    inp["beta"], self.out, Hk=wl.Hk, Hv=wl.Hv, dk=wl.d, dv=wl.d,
+                    kda=wl.variant == "kda", l2_eps=self.eps, scale=self.scale,
+                    workspace=self.workspace, stream=stream)
+        return self.out

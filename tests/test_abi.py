@@ -173,3 +173,36 @@ def test_workspace_grows_with_conv_reader_counts(lib):
     small = L.la_prefill_workspace_bytes(4, 100, 1, 4, 128, 128, 1)
     big = L.la_prefill_workspace_bytes(4, 100, 64, 64, 128, 128, 1)
     assert big > small and big % 16 == 0 and small % 16 == 0
+
+
+def _rc_decode(lib, **kw):
+    """la_decode_step with fake addresses; every case here is refused before any launch."""
+    a = dict(cs=A, hs=A, x=A, w=A, bias=None, K=4, g=A, beta=A, out=A * 2, B=4, maxb=8, Hk=1,
+             Hv=2, dk=128, dv=128, xs=512, eps=1e-6, scale=0.1, kda=0, dtype=1, ws=A * 3,
+             wsb=1 << 20)
+    a.update(kw)
+    return lib._load().la_decode_step(
+        a["cs"], a["hs"], a["x"], a["w"], a["bias"], a["K"], a["g"], a["beta"], a["out"], a["B"],
+        a["maxb"], a["Hk"], a["Hv"], a["dk"], a["dv"], a["xs"], a["eps"], a["scale"], a["kda"],
+        a["dtype"], a["ws"], a["wsb"], 0)
+
+
+def test_decode_refusals(lib):
+    assert _rc_decode(lib, B=0) == lib.LA_ERR_COUNT
+    assert _rc_decode(lib, B=9) == lib.LA_ERR_COUNT
+    assert _rc_decode(lib, dk=96, dv=96) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_decode(lib, K=0) == lib.LA_ERR_UNSUPPORTED
+    assert _rc_decode(lib, Hk=2, Hv=3) == lib.LA_ERR_ARG
+    assert _rc_decode(lib, xs=500) == lib.LA_ERR_ARG
+    assert _rc_decode(lib, x=A + 2) == lib.LA_ERR_ARG
+    assert _rc_decode(lib, hs=None) == lib.LA_ERR_ARG
+    assert _rc_decode(lib, wsb=100) == lib.LA_ERR_ARG
+    assert _rc_decode(lib, kda=3) == lib.LA_ERR_ARG
+
+
+def test_decode_workspace_size(lib):
+    L = lib._load()
+    # one bf16 conv-output row per stream, rounded up to 16 bytes
+    assert L.la_decode_workspace_bytes(3, 1, 2, 128, 128, 1) == 3 * 512 * 2
+    assert L.la_decode_workspace_bytes(3, 1, 1, 64, 64, 0) == 3 * 192 * 4
+    assert L.la_decode_workspace_bytes(0, 1, 1, 64, 64, 0) == 0
