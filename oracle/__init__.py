@@ -61,6 +61,9 @@ def _load():
                 ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_int, ctypes.c_double,
                 ctypes.c_int]
             lib.or_gated_delta_varlen.restype = None
+            lib.or_gated_rmsnorm.argtypes = [_D, _D, _D, _D, ctypes.c_long, ctypes.c_int,
+                                             ctypes.c_double]
+            lib.or_gated_rmsnorm.restype = None
             _lib = lib
     return _lib
 
@@ -112,6 +115,22 @@ def l2norm_heads(x, n_heads, head_dim, eps):
     t, C = y.shape
     if t:
         lib.or_l2norm_heads(_p(y), t, n_heads, head_dim, C, float(eps))
+    return y
+
+
+def gated_rmsnorm(o, z, w, eps):
+    """Gated RMSNorm per row of the last axis (dv): o / sqrt(mean(o^2) + eps) * w * SiLU(z).
+    o, z [..., dv] (same shape), w [dv]. Returns a new array."""
+    lib = _load()
+    o = np.ascontiguousarray(_f64(o))
+    z = np.ascontiguousarray(_f64(z))
+    w = np.ascontiguousarray(_f64(w))
+    assert o.shape == z.shape and w.shape == (o.shape[-1],)
+    y = np.empty_like(o)
+    dv = o.shape[-1]
+    n = o.size // dv if dv else 0
+    if n:
+        lib.or_gated_rmsnorm(_p(o), _p(z), _p(w), _p(y), n, dv, float(eps))
     return y
 
 

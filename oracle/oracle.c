@@ -75,6 +75,27 @@ void or_l2norm_heads(double *x, int t, int n_heads, int hd, long row_stride, dou
     }
 }
 
+/* Gated RMSNorm of the recurrence output, per (token, v-head) row of dv values
+ * ("split_prefill.rs", LayerSplitPrefill::prefill_phase3: gated RMSNorm of the GDN output with
+ * Z). The pages name the step only; read plainly:
+ *   y[c] = o[c] / sqrt(mean_c o^2 + eps) * w[c] * SiLU(z[c]),   SiLU(z) = z / (1 + e^-z),
+ * with one weight per channel (dv values) shared by all heads. o, z, y: n_rows x dv. */
+void or_gated_rmsnorm(const double *o, const double *z, const double *w, double *y, long n_rows,
+                      int dv, double eps)
+{
+    for (long r = 0; r < n_rows; ++r) {
+        const double *orow = o + (size_t)r * dv, *zrow = z + (size_t)r * dv;
+        double *yrow = y + (size_t)r * dv;
+        double ss = 0.0;
+        for (int c = 0; c < dv; ++c) ss += orow[c] * orow[c];
+        const double inv = 1.0 / sqrt(ss / dv + eps);
+        for (int c = 0; c < dv; ++c) {
+            const double gate = zrow[c] / (1.0 + exp(-zrow[c]));
+            yrow[c] = orow[c] * inv * w[c] * gate;
+        }
+    }
+}
+
 /* One (stream, v-head) unit of the gated delta rule, token by token.
  *   H  : [dk][dv] state of this v-head (in/out)
  *   q,k: rows of dk values for the unit's k-head, row strides q_stride, k_stride

@@ -9,6 +9,7 @@
   thread-count independence, and the chunked (WY) restatement == token by token.
 """
 import json
+import math
 import os
 
 import numpy as np
@@ -330,3 +331,53 @@ def test_planted_mistake_is_caught():
     out, _ = run_oracle(S0.T[None, None], q, k, v, np.zeros_like(g), beta, [4], 1.0, False)
     ob, _ = brute_unit(S0, q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], 1.0)
     assert np.max(np.abs(out[:, 0] - ob)) > 1e-3
+
+
+# ---------------------------------------------------------------- gated RMSNorm (phase-3 epilogue)
+def test_gated_rmsnorm_constant_row_closed_form():
+    """o = 3 on every channel, eps = 7: 3 / sqrt(9 + 7) = 3/4; SiLU(ln 3) = (3/4) ln 3 since
+    sigmoid(ln 3) = 3/4; with w = 2 every output is 2 (3/4)(3/4) ln 3."""
+    dv = 16
+    o = np.full((2, 3, dv), 3.0)
+    z = np.full_like(o, math.log(3.0))
+    y = oracle.gated_rmsnorm(o, z, np.full(dv, 2.0), 7.0)
+    np.testing.assert_allclose(y, 2 * 0.75 * 0.75 * math.log(3.0), rtol=1e-14)
+    y = oracle.gated_rmsnorm(-o, z, np.full(dv, 2.0), 7.0)  # odd in o
+    np.testing.assert_allclose(y, -2 * 0.75 * 0.75 * math.log(3.0), rtol=1e-14)
+
+
+def test_gated_rmsnorm_unit_rms_and_scale_invariance():
+    """eps = 0, w = 1, z = 60 (SiLU(60) = 60 to double precision): y / 60 has RMS exactly 1
+    over each row, and scaling o by c > 0 leaves y unchanged."""
+    r = rng(21)
+    dv = 128
+    o = r.standard_normal((5, 4, dv))
+    z = np.full_like(o, 60.0)
+    y = oracle.gated_rmsnorm(o, z, np.ones(dv), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean((y / 60.0) ** 2, axis=-1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.gated_rmsnorm(37.5 * o, z, np.ones(dv), 0.0), y,
+                               rtol=1e-13)
+
+
+def test_gated_rmsnorm_gate_limits_and_channel_weights():
+    """SiLU(0) = 0 and SiLU(-800) = -0: those outputs vanish; the weight scales its own channel
+    only (a transposed or shared weight would not)."""
+    r = rng(22)
+    dv = 64
+    o = r.standard_normal((3, 2, dv))
+    z = r.standard_normal((3, 2, dv))
+    z[0, 0, :] = 0.0
+    z[1, 1, :] = -800.0
+    w = r.uniform(0.5, 2.0, dv)
+    y1 = oracle.gated_rmsnorm(o, z, np.ones(dv), 1e-6)
+    yw = oracle.gated_rmsnorm(o, z, w, 1e-6)
+    assert np.all(y1[0, 0] == 0.0) and np.all(y1[1, 1] == 0.0)
+    mask = y1 != 0
+    np.testing.assert_allclose((yw[mask] / y1[mask]), np.broadcast_to(w, y1.shape)[mask],
+                               rtol=1e-14)
+    # rows are independent: changing one row's o leaves the others
+    o2 = o.copy()
+    o2[2, 0] *= -3.0
+    y2 = oracle.gated_rmsnorm(o2, z, w, 1e-6)
+    np.testing.assert_array_equal(np.delete(y2.reshape(6, dv), 4, 0),
+                                  np.delete(yw.reshape(6, dv), 4, 0))
