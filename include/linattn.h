@@ -230,6 +230,11 @@ int la_kda_prefill(const uint64_t *h_state_ptrs, const void *q, const void *k, c
  * l2_eps        x / sqrt(sum x^2 + l2_eps) per q/k head row.
  * pad_fill      KDA: value of the q/k tile rows past a stream's end before masking (as
  *               la_kda_prefill); results do not depend on it. GDN ignores it (zeros there).
+ * z, norm_w, norm_eps  optional gated RMSNorm in the output store ("split_prefill.rs",
+ *               prefill_phase3: the gated RMSNorm of the GDN output with Z): z NULL -> out = o;
+ *               else z [total_tokens][Hv][dv] and norm_w [dv] (x's dtype, 16-byte aligned) and
+ *               out = o / sqrt(mean(o^2) + norm_eps) * norm_w * SiLU(z) per (token, v-head) row,
+ *               computed from o as stored (bf16), bit for bit as la_gated_rmsnorm on that o.
  * workspace     at least la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype).
  * Covers bf16 activations with dk = dv = 128 (the tensor-core kernel) and conv_kernel 1..4;
  * anything else is LA_ERR_UNSUPPORTED (use the separate calls). Count rule:
@@ -239,8 +244,17 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
                      const float *g, const float *beta, void *out, const int32_t *cu_seqlens,
                      int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,
                      int dk, int dv, int64_t x_stride, float l2_eps, float scale, float pad_fill,
-                     int kda, int dtype, void *workspace, size_t workspace_bytes,
-                     uint64_t stream);
+                     const void *z, const void *norm_w, float norm_eps, int kda, int dtype,
+                     void *workspace, size_t workspace_bytes, uint64_t stream);
+
+/* Gated RMSNorm of a recurrence output, per (token, v-head) row of dv channels:
+ *   y = o / sqrt(mean(o^2) + eps) * w * SiLU(z),   SiLU(z) = z / (1 + e^-z).
+ * "split_prefill.rs", LayerSplitPrefill::prefill_phase3 (the gated RMSNorm of the GDN output
+ * with Z that starts phase 3); the pages name the step only, this is its plain reading.
+ * o, z, y [t][Hv][dv] contiguous (dtype; y may equal o), w [dv] (dtype); 16-byte aligned.
+ * dv in {64, 128}. Count rule: t >= 1. */
+int la_gated_rmsnorm(const void *o, const void *z, const void *w, void *y, int t, int Hv, int dv,
+                     float eps, int dtype, uint64_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Decode step: one new token for each of B streams, on the carried conv and h states (the step

@@ -68,8 +68,9 @@ _SIGS = {
                         _i32, _i32, _i32, _i64, _i64, _i64, _f32, _f32, _i32, _vp, _sz, _u64],
                        ctypes.c_int),
     "la_prefill_front": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
-                          _i32, _i32, _i32, _i32, _i32, _i64, _f32, _f32, _f32, _i32, _i32, _vp,
-                          _sz, _u64], ctypes.c_int),
+                          _i32, _i32, _i32, _i32, _i32, _i64, _f32, _f32, _f32, _vp, _vp, _f32,
+                          _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
+    "la_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _i32, _u64], ctypes.c_int),
     "la_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
     "la_decode_step": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i64, _f32, _f32, _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
@@ -261,9 +262,10 @@ def kda_prefill(h_state_ptrs, q, k, v, gate, beta, out, cu_seqlens=None, *, Hk, 
 def prefill_front(conv_state_ptrs, h_state_ptrs, x, conv_w, gate, beta, out, cu_seqlens=None, *,
                   B=None, Hk, Hv, dk, dv, kda, conv_bias=None, max_seqlen=None,
                   total_tokens=None, l2_eps=1e-6, scale=None, pad_fill=0.0, max_tokens=None,
-                  workspace=None, stream=None) -> None:
+                  z=None, norm_w=None, norm_eps=1e-6, workspace=None, stream=None) -> None:
     """conv1d + SiLU + q|k L2 + recurrence of one layer in one launch, from the pre-conv rows
-    x [tok][2*Hk*dk + Hv*dv]. cu_seqlens None: B equal streams (B defaults to 1)."""
+    x [tok][2*Hk*dk + Hv*dv]. cu_seqlens None: B equal streams (B defaults to 1). With z (and
+    norm_w [dv]) the output store applies the gated RMSNorm o/rms(o) * norm_w * SiLU(z)."""
     if cu_seqlens is not None:
         B = cu_seqlens.shape[0] - 1
     elif B is None:
@@ -277,8 +279,8 @@ def prefill_front(conv_state_ptrs, h_state_ptrs, x, conv_w, gate, beta, out, cu_
         _ptr(conv_state_ptrs), _ptr(h_state_ptrs), _ptr(x), _ptr(conv_w), _ptr(conv_bias), K,
         _ptr(gate), _ptr(beta), _ptr(out), _ptr(cu_seqlens), B, total, max_seqlen,
         max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(x),
-        float(l2_eps), float(scale), float(pad_fill), 1 if kda else 0, _dtype_code(x),
-        _ptr(workspace), ws_bytes, _stream(stream)))
+        float(l2_eps), float(scale), float(pad_fill), _ptr(z), _ptr(norm_w), float(norm_eps),
+        1 if kda else 0, _dtype_code(x), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def decode_workspace_bytes(B, Hk, Hv, dk, dv, dtype) -> int:
@@ -300,3 +302,13 @@ def decode_step(conv_state_ptrs, h_state_ptrs, x, conv_w, gate, beta, out, *, Hk
         _ptr(gate), _ptr(beta), _ptr(out), B, max_streams if max_streams is not None else B, Hk,
         Hv, dk, dv, _row_stride(x), float(l2_eps), float(scale), 1 if kda else 0,
         _dtype_code(x), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def gated_rmsnorm(o, z, w, y=None, *, eps=1e-6, stream=None):
+    """y = o / sqrt(mean(o^2) + eps) * w * SiLU(z) per row of the last axis; o, z [t][Hv][dv].
+    y defaults to o (in place). Returns y."""
+    y = o if y is None else y
+    t, Hv, dv = o.shape
+    _check(_load().la_gated_rmsnorm(_ptr(o), _ptr(z), _ptr(w), _ptr(y), t, Hv, dv, float(eps),
+                                    _dtype_code(o), _stream(stream)))
+    return y

@@ -371,8 +371,8 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
                      const float *g, const float *beta, void *out, const int32_t *cu_seqlens,
                      int B, int total_tokens, int max_seqlen, int max_tokens, int Hk, int Hv,
                      int dk, int dv, int64_t x_stride, float l2_eps, float scale, float pad_fill,
-                     int kda, int dtype, void *workspace, size_t workspace_bytes,
-                     uint64_t stream) {
+                     const void *z, const void *norm_w, float norm_eps, int kda, int dtype,
+                     void *workspace, size_t workspace_bytes, uint64_t stream) {
     if (total_tokens <= 0 || total_tokens > max_tokens)
         return fail(LA_ERR_COUNT, "prefill of %d tokens does not fit max_tokens %d", total_tokens,
                     max_tokens);
@@ -409,6 +409,12 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
     LA_TRY(check_stride(x_stride, cd, dtype, "x_stride"));
     if (x == out) return fail(LA_ERR_ARG, "out may not alias x");
     if (!(l2_eps >= 0.f)) return fail(LA_ERR_ARG, "l2_eps must be >= 0");
+    if (z) {
+        LA_TRY(check_act_ptr(z, "z"));
+        LA_TRY(check_act_ptr(norm_w, "norm_w"));
+        if (!(norm_eps >= 0.f)) return fail(LA_ERR_ARG, "norm_eps must be >= 0");
+        if (z == out) return fail(LA_ERR_ARG, "out may not alias z");
+    }
     const size_t need = la_prefill_workspace_bytes(B, total_tokens, Hk, Hv, dk, dv, dtype);
     if (workspace_bytes < need)
         return fail(LA_ERR_ARG, "workspace of %zu bytes is below the %zu required", workspace_bytes,
@@ -425,8 +431,26 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
     a.front = true;
     a.x = x; a.conv_w = conv_w; a.conv_bias = conv_bias; a.conv_state_ptrs = conv_state_ptrs;
     a.x_stride = x_stride; a.conv_k = conv_kernel; a.l2_eps = l2_eps;
+    a.z = z; a.norm_w = z ? norm_w : nullptr; a.norm_eps = norm_eps;
     a.status = status_ptr();
     return launch_result(la::launch_chunk_tc(a, as_stream(stream)), "fused prefill (tcgen05) launch");
+}
+
+int la_gated_rmsnorm(const void *o, const void *z, const void *w, void *y, int t, int Hv, int dv,
+                     float eps, int dtype, uint64_t stream) {
+    if (t <= 0) return fail(LA_ERR_COUNT, "gated rmsnorm of %d tokens", t);
+    LA_TRY(check_dtype(dtype));
+    if (dv != 64 && dv != 128)
+        return fail(LA_ERR_UNSUPPORTED, "dv %d: compiled for 64 and 128", dv);
+    if (Hv < 1) return fail(LA_ERR_ARG, "Hv must be >= 1 (got %d)", Hv);
+    LA_TRY(check_act_ptr(o, "o"));
+    LA_TRY(check_act_ptr(z, "z"));
+    LA_TRY(check_act_ptr(w, "w"));
+    LA_TRY(check_act_ptr(y, "y"));
+    if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
+    if (y == z) return fail(LA_ERR_ARG, "y may not alias z");
+    la::GatedNormArgs a{o, z, w, y, t, Hv, dv, eps, dtype};
+    return launch_result(la::launch_gated_rmsnorm(a, as_stream(stream)), "gated rmsnorm launch");
 }
 
 size_t la_decode_workspace_bytes(int B, int Hk, int Hv, int dk, int dv, int dtype) {

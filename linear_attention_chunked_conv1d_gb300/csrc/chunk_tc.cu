@@ -1018,9 +1018,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 for (int m = 0; m < 1024 / TC_THREADS; ++m) {
                     const int idx = tid + TC_THREADS * m;  // 0..1023
                     const int t = idx >> 4, cj = idx & 15;
-                    if (t < n)
-                        *reinterpret_cast<uint4 *>(og + (int64_t)(tok0 + t) * Hv * TC_D + cj * 8) =
-                            *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
+                    __nv_bfloat16 *dst = og + (int64_t)(tok0 + t) * Hv * TC_D + cj * 8;
+                    if (a.z) {
+                        // gated RMSNorm of the stored (bf16) o row: 16 lanes x 8 channels, the
+                        // order of the separate gated-norm kernel
+                        float ov[8];
+                        Vec16<__nv_bfloat16>::load(os + t * O_LD + cj * 8, ov);
+                        float ss = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(ov[e], ov[e], ss);
+#pragma unroll
+                        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                        if (t < n) {
+                            float zv[8], wv[8];
+                            Vec16<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(a.z) +
+                                                           ((int64_t)(tok0 + t) * Hv + j) * TC_D + cj * 8, zv);
+                            Vec16<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(a.norm_w) + cj * 8, wv);
+                            const float inv = rsqrtf(ss * (1.f / TC_D) + a.norm_eps);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) ov[e] = ov[e] * inv * wv[e] * silu(zv[e]);
+                            Vec16<__nv_bfloat16>::store(dst, ov);
+                        }
+                    } else if (t < n) {
+                        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
+                    }
                 }
             }
             tc::fence_before_sync();

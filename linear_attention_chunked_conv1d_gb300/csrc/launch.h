@@ -57,6 +57,10 @@ struct RecArgs {
     int64_t x_stride;
     int conv_k;
     float l2_eps;
+    // Gated RMSNorm in the output store (tensor-core kernel only): when z is set, out receives
+    // o / sqrt(mean(o^2) + norm_eps) * norm_w * SiLU(z) per (token, v-head) row, from the bf16 o.
+    const void *z, *norm_w;
+    float norm_eps;
 };
 // CUDA-core chunked kernel (fp32 and bf16 activations, head dims 64 and 128).
 cudaError_t launch_chunk_simt(const RecArgs &a, cudaStream_t st);
@@ -86,5 +90,16 @@ struct DecArgs {
     bool kda;
 };
 cudaError_t launch_decode_recurrence(const DecArgs &a, cudaStream_t st);
+
+// Gated RMSNorm y = o / sqrt(mean(o^2) + eps) * w * SiLU(z) per row of dv channels; o, z, y
+// [t][Hv][dv] contiguous (y may be o), w [dv].
+struct GatedNormArgs {
+    const void *o, *z, *w;
+    void *y;
+    int t, Hv, dv;
+    float eps;
+    int dtype;
+};
+cudaError_t launch_gated_rmsnorm(const GatedNormArgs &a, cudaStream_t st);
 
 }  // namespace la

@@ -139,13 +139,14 @@ def _rc_front(lib, **kw):
     """la_prefill_front with fake addresses; every case here is refused before any launch."""
     a = dict(cs=A, hs=A, x=A, w=A, bias=None, K=4, g=A, beta=A, out=A * 2, cu=A, B=2, total=40,
              max_seqlen=30, max_tokens=100, Hk=1, Hv=2, dk=128, dv=128, xs=512, eps=1e-6,
-             scale=0.1, pad=0.0, kda=0, dtype=1, ws=A * 3, wsb=1 << 20)
+             scale=0.1, pad=0.0, z=None, nw=None, neps=1e-6, kda=0, dtype=1, ws=A * 3,
+             wsb=1 << 20)
     a.update(kw)
     return lib._load().la_prefill_front(
         a["cs"], a["hs"], a["x"], a["w"], a["bias"], a["K"], a["g"], a["beta"], a["out"],
         a["cu"], a["B"], a["total"], a["max_seqlen"], a["max_tokens"], a["Hk"], a["Hv"], a["dk"],
-        a["dv"], a["xs"], a["eps"], a["scale"], a["pad"], a["kda"], a["dtype"], a["ws"],
-        a["wsb"], 0)
+        a["dv"], a["xs"], a["eps"], a["scale"], a["pad"], a["z"], a["nw"], a["neps"], a["kda"],
+        a["dtype"], a["ws"], a["wsb"], 0)
 
 
 def test_fused_prefill_refusals(lib):
@@ -166,6 +167,20 @@ def test_fused_prefill_refusals(lib):
     assert _rc_front(lib, wsb=16) == lib.LA_ERR_ARG                   # workspace too small
     assert _rc_front(lib, ws=None) == lib.LA_ERR_ARG
     assert "workspace" in lib.last_error()
+    assert _rc_front(lib, z=A * 4, nw=None) == lib.LA_ERR_ARG          # gated norm: weight needed
+    assert _rc_front(lib, z=A * 4 + 2, nw=A * 5) == lib.LA_ERR_ARG     # misaligned z
+    assert _rc_front(lib, z=A * 4, nw=A * 5, neps=-1.0) == lib.LA_ERR_ARG
+
+
+def test_gated_rmsnorm_refusals(lib):
+    f = lib._load().la_gated_rmsnorm
+    assert f(A, A * 2, A * 3, A * 4, 0, 2, 128, 1e-6, 1, 0) == lib.LA_ERR_COUNT
+    assert f(A, A * 2, A * 3, A * 4, 5, 2, 96, 1e-6, 1, 0) == lib.LA_ERR_UNSUPPORTED
+    assert f(A, A * 2, A * 3, A * 4, 5, 0, 128, 1e-6, 1, 0) == lib.LA_ERR_ARG
+    assert f(A + 2, A * 2, A * 3, A * 4, 5, 2, 128, 1e-6, 1, 0) == lib.LA_ERR_ARG
+    assert f(A, A * 2, None, A * 4, 5, 2, 128, 1e-6, 1, 0) == lib.LA_ERR_ARG
+    assert f(A, A * 2, A * 3, A * 2, 5, 2, 128, 1e-6, 1, 0) == lib.LA_ERR_ARG   # y aliases z
+    assert f(A, A * 2, A * 3, A * 4, 5, 2, 128, -1.0, 1, 0) == lib.LA_ERR_ARG
 
 
 def test_workspace_grows_with_conv_reader_counts(lib):
