@@ -102,16 +102,18 @@ def kernel_source_sha(name: str) -> str:
         return hashlib.sha1(f.read()).hexdigest()[:12]
 
 
-def profiled_traffic(kernel_file: str, workload: str):
+def profiled_traffic(kernel_file: str, workload: str, kind: str):
     """DRAM bytes (read + write) per launch from profiles/traffic.txt, only if the kernel source
-    is unchanged since the counters were taken (lines: file workload sha12 bytes)."""
+    is unchanged since the counters were taken (lines: file workload sha12 bytes kind, kind
+    'fused' for the one-launch layer kernel, 'split' for the recurrence of the two-launch path)."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     sha = kernel_source_sha(kernel_file)
     for line in open(p):
         parts = line.split()
-        if len(parts) == 4 and parts[0] == kernel_file and parts[1] == workload and parts[2] == sha:
+        if (len(parts) == 5 and parts[0] == kernel_file and parts[1] == workload
+                and parts[2] == sha and parts[4] == kind):
             return int(parts[3])
     return None
 
@@ -413,7 +415,7 @@ def main():
     tc = uses_tensor_cores(wl)
     kernel_file = "chunk_tc.cu" if tc else "chunk_simt.cu"
     kernel_name = "chunk_tc_kernel" if tc else "chunk_simt_kernel"
-    traffic = profiled_traffic(kernel_file, wl.name)
+    traffic = profiled_traffic(kernel_file, wl.name, "fused" if use_fused else "split")
     # fused: stream order + layer kernel; else conv(+L2), (stream order), recurrence
     launches_per_step = 2 if use_fused else (3 if tc else 2)
     line = {
