@@ -503,6 +503,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
         }
 
+        // Global stores of a chunk's output tile, staged as bf16 [t][d] in the A^T buffer; they
+        // are issued in the next chunk while its first MMAs run (or after the last chunk).
+        auto store_o = [&](int tok0s, int ns) {
+            const __nv_bfloat16 *os = reinterpret_cast<const __nv_bfloat16 *>(sm + SM_AT);
+#pragma unroll
+            for (int m = 0; m < 1024 / TC_THREADS; ++m) {
+                const int idx = tid + TC_THREADS * m;  // 0..1023
+                const int t = idx >> 4, cj = idx & 15;
+                __nv_bfloat16 *dst = og + (int64_t)(tok0s + t) * Hv * TC_D + cj * 8;
+                if (a.z) {
+                    // gated RMSNorm of the stored (bf16) o row: 16 lanes x 8 channels, the
+                    // order of the separate gated-norm kernel
+                    float ov[8];
+                    Vec16<__nv_bfloat16>::load(os + t * O_LD + cj * 8, ov);
+                    float ss = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(ov[e], ov[e], ss);
+#pragma unroll
+                    for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                    if (t < ns) {
+                        float zv[8], wv[8];
+                        Vec16<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(a.z) +
+                                                       ((int64_t)(tok0s + t) * Hv + j) * TC_D + cj * 8, zv);
+                        Vec16<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(a.norm_w) + cj * 8, wv);
+                        const float inv = rsqrtf(ss * (1.f / TC_D) + a.norm_eps);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ov[e] = ov[e] * inv * wv[e] * silu(zv[e]);
+                        Vec16<__nv_bfloat16>::store(dst, ov);
+                    }
+                } else if (t < ns) {
+                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
+                }
+            }
+        };
+        int pend_tok0 = 0, pend_n = 0;  // output tile staged, not yet stored
+
         for (int ch = 0; ch < nch; ++ch) {
             const int tok0 = t0 + ch * TC_C;
             const int n = min(TC_C, len - ch * TC_C);
@@ -537,6 +573,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             cp_async_wait_all();
             tc::fence_async_smem();
             if (!sync_ok(err)) break;
+            // this chunk's scalar gates are in shared memory: fetch the next chunk's
+            if (!last) fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
             if (KDA) {
                 float carry = 0.f;
 #pragma unroll
@@ -684,6 +722,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 issue_mma2();
             }
 
+            if (pend_n > 0) {  // previous chunk's output while D1 is computed
+                store_o(pend_tok0, pend_n);
+                pend_n = 0;
+            }
+
             // ---------------- D1 ready (or computed exactly on CUDA cores, KDA fallback)
             if (!slow) {
                 wait_bar(bar_a, phase_a);
@@ -718,6 +761,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 tc::fence_after_sync();
             }
             if (!sync_ok(err)) break;
+            if (!KDA && !FRONT && !last) {  // GDN: K|Q tile consumed (D1, K^T, staging)
+                load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+                cp_async_commit();
+            }
 
             // ---------------- A^T (fp32) and P (tf32) from D1; GDN: K^T tile
             {
@@ -838,12 +885,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
             tc::fence_async_smem();
             __syncthreads();
-            if (!last) {  // K|Q tile is free: next chunk's K, Q (and gates) in flight
-                if (!FRONT) {
+            if (!last) {  // KDA: K|Q tile consumed by the staging: next chunk's K, Q and gates
+                if (KDA && !FRONT) {
                     load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                     cp_async_commit();
                 }
-                fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
                 if (KDA) {
                     const int nn = min(TC_C, len - (ch + 1) * TC_C);
                     const float *gp = a.g + ((int64_t)(tok0 + TC_C) * Hv + j) * TC_D + row;
@@ -999,7 +1045,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             if (!sync_ok(err)) break;
 
             // ---------------- o = scale (e^gc (Q H) + P U'): staged as bf16 [t][d] in shared
-            //                  memory, then written with 16-byte stores, rows < n
+            //                  memory; written with 16-byte stores (rows < n) in the next chunk
             {
                 __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + SM_AT);
                 const int t0c = C16 * part;
@@ -1013,42 +1059,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     const float o = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
                     os[t * O_LD + row] = __float2bfloat16_rn(scale * o);
                 }
-                __syncthreads();
-#pragma unroll
-                for (int m = 0; m < 1024 / TC_THREADS; ++m) {
-                    const int idx = tid + TC_THREADS * m;  // 0..1023
-                    const int t = idx >> 4, cj = idx & 15;
-                    __nv_bfloat16 *dst = og + (int64_t)(tok0 + t) * Hv * TC_D + cj * 8;
-                    if (a.z) {
-                        // gated RMSNorm of the stored (bf16) o row: 16 lanes x 8 channels, the
-                        // order of the separate gated-norm kernel
-                        float ov[8];
-                        Vec16<__nv_bfloat16>::load(os + t * O_LD + cj * 8, ov);
-                        float ss = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) ss = fmaf(ov[e], ov[e], ss);
-#pragma unroll
-                        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                        if (t < n) {
-                            float zv[8], wv[8];
-                            Vec16<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(a.z) +
-                                                           ((int64_t)(tok0 + t) * Hv + j) * TC_D + cj * 8, zv);
-                            Vec16<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(a.norm_w) + cj * 8, wv);
-                            const float inv = rsqrtf(ss * (1.f / TC_D) + a.norm_eps);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) ov[e] = ov[e] * inv * wv[e] * silu(zv[e]);
-                            Vec16<__nv_bfloat16>::store(dst, ov);
-                        }
-                    } else if (t < n) {
-                        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
-                    }
-                }
+                pend_tok0 = tok0;
+                pend_n = n;
             }
             tc::fence_before_sync();
             __syncthreads();
             tc::fence_after_sync();
         }
         if (*err) break;
+        if (pend_n > 0) {  // the last chunk's output (staged before the barrier above)
+            store_o(pend_tok0, pend_n);
+            pend_n = 0;
+        }
 
         // state back: H[c][d] = S[d][c]
 #pragma unroll
