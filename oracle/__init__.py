@@ -5,8 +5,9 @@ import this package. The product library (``linear_attention_chunked_conv1d_gb30
 imports, links or calls it, and the two share no code.
 
 The arithmetic lives in ``oracle.c`` (plain sequential C, fp64, one host thread per
-(stream, v-head) unit); this module only marshals numpy float64 arrays into it and composes
-the steps in the order the pages launch them ("glm5next_kda/prefill.rs",
+(stream, v-head) unit), except the phase-1 projection and its row norm (``linear``,
+``rmsnorm_rows``), written here in fp64 numpy around one matrix product; this module marshals
+numpy float64 arrays into the C code and composes the steps in the order the pages launch them ("glm5next_kda/prefill.rs",
 ``Glm5NextKdaLayer::prefill_with_pad_fill``: conv_prefill -> l2 -> chunk_prepare/chunk_scan).
 
 Reading of the pages (where they are silent): activations produced by the front end are
@@ -132,6 +133,21 @@ def gated_rmsnorm(o, z, w, eps):
     if n:
         lib.or_gated_rmsnorm(_p(o), _p(z), _p(w), _p(y), n, dv, float(eps))
     return y
+
+
+def linear(a, w):
+    """Phase-1 projection of a batch of rows ("split_prefill.rs",
+    LayerSplitPrefill::prefill_phase1_proj_batched: the QKVZ and gate projections of the
+    normalised hidden rows): C = A W^T in fp64, with A [M][K] and W [N][K] in the [out][in]
+    layout of a linear layer. The matrix product is the library primitive of this step."""
+    return _f64(a) @ _f64(w).T
+
+
+def rmsnorm_rows(x, w, eps):
+    """The norm of phase 1: y = x / sqrt(mean(x^2) + eps) * w per row (fp64)."""
+    x = _f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * _f64(w)
 
 
 def gated_delta(h_states, q, k, v, g, beta, cu_seqlens, *, scale, per_channel=False,

@@ -381,3 +381,36 @@ def test_gated_rmsnorm_gate_limits_and_channel_weights():
     y2 = oracle.gated_rmsnorm(o2, z, w, 1e-6)
     np.testing.assert_array_equal(np.delete(y2.reshape(6, dv), 4, 0),
                                   np.delete(yw.reshape(6, dv), 4, 0))
+
+
+# ---------------------------------------------------------------- phase-1 projection and norm
+def test_linear_brute_force_and_closed_forms():
+    r = rng(31)
+    a = r.standard_normal((5, 7))
+    w = r.standard_normal((4, 7))
+    c = oracle.linear(a, w)
+    brute = [[sum(a[m, k] * w[n, k] for k in range(7)) for n in range(4)] for m in range(5)]
+    np.testing.assert_allclose(c, brute, rtol=1e-13, atol=1e-13)
+    assert c.shape == (5, 4)
+    # A = I picks the rows of W as columns; a rank-one A = u v^T gives u (W v)^T
+    np.testing.assert_array_equal(oracle.linear(np.eye(7), w), w.T)
+    u, v = r.standard_normal(5), r.standard_normal(7)
+    np.testing.assert_allclose(oracle.linear(np.outer(u, v), w), np.outer(u, w @ v), rtol=1e-12)
+    # zero columns appended to both operands (a K tail) change nothing
+    a0 = np.concatenate([a, np.zeros((5, 9))], axis=1)
+    w0 = np.concatenate([w, r.standard_normal((4, 9)) * 0], axis=1)
+    np.testing.assert_array_equal(oracle.linear(a0, w0), c)
+
+
+def test_rmsnorm_rows_closed_forms():
+    # constant row 3 with eps = 7: 3 / sqrt(9 + 7) = 0.75; unit RMS at eps = 0; scale invariance
+    x = np.full((2, 8), 3.0)
+    np.testing.assert_allclose(oracle.rmsnorm_rows(x, np.full(8, 2.0), 7.0), 1.5, rtol=1e-15)
+    r = rng(32)
+    x = r.standard_normal((6, 64))
+    y = oracle.rmsnorm_rows(x, np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.rmsnorm_rows(5.5 * x, np.ones(64), 0.0), y, rtol=1e-13)
+    w = r.uniform(0.5, 2, 64)
+    np.testing.assert_allclose(oracle.rmsnorm_rows(x, w, 0.0) / y, np.broadcast_to(w, y.shape),
+                               rtol=1e-13)
