@@ -32,12 +32,13 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from linear_attention_chunked_conv1d_gb300.inputs import (  # noqa: E402
-    DECODE_WORKLOADS, WORKLOADS, make_inputs)
+    DECODE_WORKLOADS, PROJ_WORKLOADS, WORKLOADS, make_inputs)
 
 DEFAULT_WORKLOAD = "gdn_batched_8x2048_h16_d128"
 METRIC = "prefill tokens/s per GDN/KDA layer"
 DECODE_METRIC = "decode tokens/s per GDN/KDA layer"
-ALL_WORKLOADS = {**WORKLOADS, **DECODE_WORKLOADS}
+PROJ_METRIC = "phase-1 projection tokens/s (QKVZ GEMM)"
+ALL_WORKLOADS = {**WORKLOADS, **DECODE_WORKLOADS, **PROJ_WORKLOADS}
 CHUNK = 64
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -311,6 +312,9 @@ def main():
         pg = dist
 
     la._load()
+    if wl.mode == "proj":
+        run_proj(args, wl, dev, local, rank, world, pg)
+        return
     inp = make_inputs(wl, device=dev, seed=rank)  # each replica its own batch (weak scaling)
     if wl.mode == "decode":
         run_decode(args, wl, inp, dev, local, rank, world, pg)
@@ -462,6 +466,94 @@ def main():
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def run_proj(args, wl, dev, local, rank, world, pg):
+    """One step = the QKVZ projection GEMM of the stacked tokens (la_gemm_bf16), operands in
+    HBM; tensor-bound. torch.matmul (cuBLAS) on the same operands is timed beside it."""
+    import linear_attention_chunked_conv1d_gb300 as la
+    T = wl.B * int(wl.lengths.split(":")[1])
+    Kd, N = wl.hidden, 4 * wl.Hv * wl.d
+    gen = torch.Generator(dev)
+    gen.manual_seed(rank)
+    a = torch.randn(T, Kd, generator=gen, device=dev).to(torch.bfloat16)
+    w = (torch.randn(N, Kd, generator=gen, device=dev) / math.sqrt(Kd)).to(torch.bfloat16)
+    c = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+
+    if pg:
+        pg.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_ours = timed(lambda: la.gemm_bf16(a, w, c))
+    clk = clocks.stop()
+    ms_cublas = timed(lambda: torch.matmul(a, w.t(), out=c))
+    value, ms, _ = aggregate(T, ms_ours, pg, dev)
+    # end to end: the hidden rows in from pinned host memory, the projection out
+    a_h = a.cpu().pin_memory()
+    c_h = torch.empty(c.shape, dtype=c.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        a.copy_(a_h, non_blocking=True)
+        la.gemm_bf16(a, w, c)
+        c_h.copy_(c, non_blocking=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        a.copy_(a_h, non_blocking=True)
+        la.gemm_bf16(a, w, c)
+        c_h.copy_(c, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_value, _, _ = aggregate(T, e0.elapsed_time(e1) / args.steps, pg, dev)
+    if rank != 0:
+        if pg:
+            pg.barrier()
+            pg.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    flops = 2.0 * T * N * Kd
+    achieved = flops / (ms_ours * 1e-3) / 1e12
+    line = {
+        "metric": PROJ_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; hidden rows ~N(0,1), weights ~N(0,1/hidden))",
+        "config": {"workload": wl.name, "tokens_per_step": T, "hidden": Kd, "outputs": N,
+                   "path": "la_gemm_bf16 (tcgen05 + TMA, 128x256 tiles, fp32 accumulation)",
+                   "l2": "flushed between timed steps (write of a 258 MiB buffer)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": a_h.numel() * 2,
+                "d2h_bytes_per_step": c_h.numel() * 2},
+        "roofline": {"bound": "tensor", "kernel": "gemm_bf16_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops (burst: the kernel is timed alone)",
+                     "flops_per_launch": flops, "avg_launch_ms": ms_ours},
+        "cublas_same_shape": {"ms": ms_cublas,
+                              "tflops": flops / (ms_cublas * 1e-3) / 1e12,
+                              "note": "torch.matmul on the same operands, context only"},
+    }
     print(json.dumps(line), flush=True)
     if pg:
         pg.barrier()

@@ -280,6 +280,17 @@ int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs
                    int Hv, int dk, int dv, int64_t x_stride, float l2_eps, float scale, int kda,
                    int dtype, void *workspace, size_t workspace_bytes, uint64_t stream);
 
+/* Phase-1 projection GEMM: C[M][N] = A[M][K] W[N][K]^T. "split_prefill.rs",
+ * LayerSplitPrefill::prefill_phase1_proj_batched (the QKVZ and gate projections of all stacked
+ * tokens of a batched prefill, on the normalised hidden rows).
+ * a, w, c       bf16, row-major with row strides lda, ldw, ldc (elements, multiples of 8, at
+ *               least K, K, N); 16-byte aligned; c may not overlap a or w. w is a linear layer's
+ *               weight in its [out][in] layout.
+ * Tensor cores (tcgen05, TMA), fp32 accumulation, the output rounded to bf16 once.
+ * Count rule: M, N, K >= 1. */
+int la_gemm_bf16(const void *a, const void *w, void *c, int M, int N, int K, int64_t lda,
+                 int64_t ldw, int64_t ldc, uint64_t stream);
+
 #ifdef __cplusplus
 }
 #endif

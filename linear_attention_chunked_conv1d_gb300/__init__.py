@@ -71,6 +71,7 @@ _SIGS = {
                           _i32, _i32, _i32, _i32, _i32, _i64, _f32, _f32, _f32, _vp, _vp, _f32,
                           _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
     "la_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _i32, _u64], ctypes.c_int),
+    "la_gemm_bf16": ([_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _i64, _u64], ctypes.c_int),
     "la_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
     "la_decode_step": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i64, _f32, _f32, _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
@@ -312,3 +313,15 @@ def gated_rmsnorm(o, z, w, y=None, *, eps=1e-6, stream=None):
     _check(_load().la_gated_rmsnorm(_ptr(o), _ptr(z), _ptr(w), _ptr(y), t, Hv, dv, float(eps),
                                     _dtype_code(o), _stream(stream)))
     return y
+
+
+def gemm_bf16(a, w, c=None, *, stream=None):
+    """C = A W^T (bf16, fp32 accumulation on the tensor cores); a [M][K], w [N][K] (a linear
+    layer's [out][in] weight); c [M][N] (allocated when None). Returns c."""
+    M, K = a.shape
+    N = w.shape[0]
+    if c is None:
+        c = torch.empty(M, N, dtype=torch.bfloat16, device=a.device)
+    _check(_load().la_gemm_bf16(_ptr(a), _ptr(w), _ptr(c), M, N, K, _row_stride(a),
+                                _row_stride(w), _row_stride(c), _stream(stream)))
+    return c

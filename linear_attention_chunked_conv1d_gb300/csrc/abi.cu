@@ -515,4 +515,25 @@ int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs
     return launch_result(la::launch_decode_recurrence(d, st), "decode recurrence launch");
 }
 
+int la_gemm_bf16(const void *a, const void *w, void *c, int M, int N, int K, int64_t lda,
+                 int64_t ldw, int64_t ldc, uint64_t stream) {
+    if (M < 1 || N < 1 || K < 1)
+        return fail(LA_ERR_COUNT, "gemm of %d x %d x %d", M, N, K);
+    LA_TRY(check_act_ptr(a, "a"));
+    LA_TRY(check_act_ptr(w, "w"));
+    LA_TRY(check_act_ptr(c, "c"));
+    LA_TRY(check_stride(lda, K, LA_BF16, "lda"));
+    LA_TRY(check_stride(ldw, K, LA_BF16, "ldw"));
+    LA_TRY(check_stride(ldc, N, LA_BF16, "ldc"));
+    const char *cb = static_cast<const char *>(c), *ce = cb + ((int64_t)(M - 1) * ldc + N) * 2;
+    auto overlaps = [&](const void *p, int64_t rows, int64_t ld, int64_t cols) {
+        const char *pb = static_cast<const char *>(p), *pe = pb + ((rows - 1) * ld + cols) * 2;
+        return pb < ce && cb < pe;
+    };
+    if (overlaps(a, M, lda, K) || overlaps(w, N, ldw, K))
+        return fail(LA_ERR_ARG, "c may not overlap a or w");
+    la::GemmArgs g{a, w, c, M, N, K, lda, ldw, ldc, status_ptr()};
+    return launch_result(la::launch_gemm_bf16(g, as_stream(stream)), "gemm (tcgen05) launch");
+}
+
 }  // extern "C"

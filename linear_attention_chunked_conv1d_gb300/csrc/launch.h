@@ -102,4 +102,14 @@ struct GatedNormArgs {
 };
 cudaError_t launch_gated_rmsnorm(const GatedNormArgs &a, cudaStream_t st);
 
+// Projection GEMM C[M][N] = A[M][K] W[N][K]^T, bf16 in and out, fp32 accumulation (tcgen05).
+struct GemmArgs {
+    const void *a, *w;
+    void *c;
+    int M, N, K;
+    int64_t lda, ldw, ldc;
+    int *status;
+};
+cudaError_t launch_gemm_bf16(const GemmArgs &a, cudaStream_t st);
+
 }  // namespace la

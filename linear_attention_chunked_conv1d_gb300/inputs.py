@@ -35,7 +35,9 @@ class Workload:
     x_std: float = 1.0
     w_std: float = 0.25
     batched: bool = False      # equal-length streams through the batched call
-    mode: str = "prefill"      # "prefill", or "decode": one new token per stream (lengths fixed:1)
+    mode: str = "prefill"      # "prefill", "decode" (one new token per stream, lengths fixed:1)
+                               # or "proj" (the phase-1 projection GEMM of the stacked tokens)
+    hidden: int = 0            # proj: width of the hidden rows (the GEMM's K)
 
     @property
     def cd(self) -> int:
@@ -175,3 +177,10 @@ def recurrence_inputs(B_lengths, Hk, Hv, d, *, kda=False, dtype="bf16", seed=0, 
     out = dict(q=q.to(act), k=k.to(act), v=v.to(act), h=h, g=g, beta=beta, cu_seqlens=cu,
                lengths=list(B_lengths))
     return {k_: (v_.to(device) if torch.is_tensor(v_) else v_) for k_, v_ in out.items()}
+
+# Phase-1 projection (QKVZ) of the stacked tokens of the batched GDN prefill: 16384 tokens,
+# hidden 2048 -> q | k | v | z = 4 x 16 heads x 128 = 8192 outputs, bf16, random weights.
+PROJ_WORKLOADS = {
+    "proj_qkvz_16384x2048x8192": Workload("proj_qkvz_16384x2048x8192", "gdn", 8, 16, 16, 128,
+                                          "fixed:2048", mode="proj", hidden=2048),
+}

@@ -221,3 +221,15 @@ def test_decode_workspace_size(lib):
     assert L.la_decode_workspace_bytes(3, 1, 2, 128, 128, 1) == 3 * 512 * 2
     assert L.la_decode_workspace_bytes(3, 1, 1, 64, 64, 0) == 3 * 192 * 4
     assert L.la_decode_workspace_bytes(0, 1, 1, 64, 64, 0) == 0
+
+
+def test_gemm_refusals(lib):
+    f = lib._load().la_gemm_bf16
+    B = A * 16
+    assert f(A, B, A * 64, 0, 8, 8, 8, 8, 8, 0) == lib.LA_ERR_COUNT
+    assert f(A, B, A * 64, 8, 8, 0, 8, 8, 8, 0) == lib.LA_ERR_COUNT
+    assert f(A + 2, B, A * 64, 8, 8, 8, 8, 8, 8, 0) == lib.LA_ERR_ARG       # misaligned
+    assert f(A, B, A * 64, 8, 8, 16, 8, 16, 8, 0) == lib.LA_ERR_ARG         # lda < K
+    assert f(A, B, A * 64, 8, 8, 12, 12, 16, 8, 0) == lib.LA_ERR_ARG        # lda not 16 B
+    assert f(A, B, A * 64, 8, 16, 8, 8, 8, 8, 0) == lib.LA_ERR_ARG          # ldc < N
+    assert f(A, B, A + 64, 8, 8, 8, 8, 8, 8, 0) == lib.LA_ERR_ARG           # c overlaps a
