@@ -150,6 +150,14 @@ def rmsnorm_rows(x, w, eps):
     return x / np.sqrt(ms + eps) * _f64(w)
 
 
+def gate_activations(a, b):
+    """The gates of phase 1 from their projections: g = -softplus(a) = -log(1 + e^a) (the
+    log-decay, <= 0) and beta = sigmoid(b) = 1 / (1 + e^-b), in fp64. This is the plain reading
+    of "gates" in prefill_phase1_proj_batched, and the transform of the synthetic input recipe."""
+    a, b = _f64(a), _f64(b)
+    return -np.logaddexp(0.0, a), 1.0 / (1.0 + np.exp(-b))
+
+
 def gated_delta(h_states, q, k, v, g, beta, cu_seqlens, *, scale, per_channel=False,
                 threads=None):
     """Token-by-token gated delta rule over packed streams.

@@ -414,3 +414,18 @@ def test_rmsnorm_rows_closed_forms():
     w = r.uniform(0.5, 2, 64)
     np.testing.assert_allclose(oracle.rmsnorm_rows(x, w, 0.0) / y, np.broadcast_to(w, y.shape),
                                rtol=1e-13)
+
+
+def test_gate_activations_closed_forms():
+    """softplus(0) = ln 2, softplus(ln 3) = ln 4, softplus(a) -> a for large a and -> e^a for very
+    negative a; sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, sigmoid(-b) = 1 - sigmoid(b)."""
+    a = np.array([0.0, math.log(3.0), 60.0, -60.0, 800.0])
+    b = np.array([0.0, math.log(3.0), -2.5, 2.5, -800.0])
+    g, beta = oracle.gate_activations(a, b)
+    np.testing.assert_allclose(g[:2], [-math.log(2.0), -math.log(4.0)], rtol=1e-15)
+    np.testing.assert_allclose(g[2], -60.0, rtol=1e-15)
+    np.testing.assert_allclose(g[3], -math.exp(-60.0), rtol=1e-12)
+    assert g[4] == -800.0 and np.all(g <= 0)
+    np.testing.assert_allclose(beta[:2], [0.5, 0.75], rtol=1e-15)
+    np.testing.assert_allclose(beta[2] + beta[3], 1.0, rtol=1e-15)
+    assert beta[4] == 0.0
