@@ -291,6 +291,20 @@ int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs
 int la_gemm_bf16(const void *a, const void *w, void *c, int M, int N, int K, int64_t lda,
                  int64_t ldw, int64_t ldc, uint64_t stream);
 
+/* The norm of phase 1: y = x / sqrt(mean(x^2) + eps) * w per row of `width` channels (bf16).
+ * "split_prefill.rs", prefill_phase1_proj_batched ("projections (norm, QKVZ, gates)"): the
+ * norm of the hidden rows that the projection GEMM reads. x [rows][ldx], y [rows][ldy] (may be
+ * x), w [width]; 16-byte aligned; width a multiple of 8 up to 8192; strides multiples of 8.
+ * Count rule: rows >= 1. */
+int la_rmsnorm_rows(const void *x, const void *w, void *y, int rows, int width, int64_t ldx,
+                    int64_t ldy, float eps, uint64_t stream);
+
+/* The gates of phase 1 from the gate projection rows ab [t][ld] (bf16, columns a | b):
+ * g = -softplus(a) [t][na] and beta = sigmoid(b) [t][nb], fp32 (na = Hv for GDN, Hv*dk for KDA;
+ * nb = Hv). "split_prefill.rs", prefill_phase1_proj_batched ("gates"). Count rule: t >= 1. */
+int la_gate_activations(const void *ab, int64_t ld, int t, int na, int nb, float *g,
+                        float *beta, uint64_t stream);
+
 #ifdef __cplusplus
 }
 #endif

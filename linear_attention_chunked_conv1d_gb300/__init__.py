@@ -72,6 +72,8 @@ _SIGS = {
                           _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
     "la_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _i32, _u64], ctypes.c_int),
     "la_gemm_bf16": ([_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _i64, _u64], ctypes.c_int),
+    "la_rmsnorm_rows": ([_vp, _vp, _vp, _i32, _i32, _i64, _i64, _f32, _u64], ctypes.c_int),
+    "la_gate_activations": ([_vp, _i64, _i32, _i32, _i32, _vp, _vp, _u64], ctypes.c_int),
     "la_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
     "la_decode_step": ([_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
                         _i32, _i32, _i64, _f32, _f32, _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
@@ -325,3 +327,26 @@ def gemm_bf16(a, w, c=None, *, stream=None):
     _check(_load().la_gemm_bf16(_ptr(a), _ptr(w), _ptr(c), M, N, K, _row_stride(a),
                                 _row_stride(w), _row_stride(c), _stream(stream)))
     return c
+
+
+def rmsnorm_rows(x, w, y=None, *, eps=1e-6, stream=None):
+    """y = x / sqrt(mean(x^2) + eps) * w per row (bf16); y defaults to a new tensor."""
+    rows, width = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    _check(_load().la_rmsnorm_rows(_ptr(x), _ptr(w), _ptr(y), rows, width, _row_stride(x),
+                                   _row_stride(y), float(eps), _stream(stream)))
+    return y
+
+
+def gate_activations(ab, na, g=None, beta=None, *, stream=None):
+    """g = -softplus(ab[:, :na]), beta = sigmoid(ab[:, na:]) in fp32 (new tensors by default)."""
+    t, width = ab.shape
+    nb = width - na
+    if g is None:
+        g = torch.empty(t, na, dtype=torch.float32, device=ab.device)
+    if beta is None:
+        beta = torch.empty(t, nb, dtype=torch.float32, device=ab.device)
+    _check(_load().la_gate_activations(_ptr(ab), _row_stride(ab), t, na, nb, _ptr(g), _ptr(beta),
+                                       _stream(stream)))
+    return g, beta

@@ -536,4 +536,30 @@ int la_gemm_bf16(const void *a, const void *w, void *c, int M, int N, int K, int
     return launch_result(la::launch_gemm_bf16(g, as_stream(stream)), "gemm (tcgen05) launch");
 }
 
+int la_rmsnorm_rows(const void *x, const void *w, void *y, int rows, int width, int64_t ldx,
+                    int64_t ldy, float eps, uint64_t stream) {
+    if (rows < 1) return fail(LA_ERR_COUNT, "rmsnorm of %d rows", rows);
+    if (width < 8 || width % 8 || width > la::rmsnorm_rows_max_width())
+        return fail(LA_ERR_UNSUPPORTED, "width %d: a multiple of 8 up to %d", width,
+                    la::rmsnorm_rows_max_width());
+    LA_TRY(check_act_ptr(x, "x"));
+    LA_TRY(check_act_ptr(w, "w"));
+    LA_TRY(check_act_ptr(y, "y"));
+    LA_TRY(check_stride(ldx, width, LA_BF16, "ldx"));
+    LA_TRY(check_stride(ldy, width, LA_BF16, "ldy"));
+    if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
+    la::RowNormArgs a{x, w, y, rows, width, ldx, ldy, eps};
+    return launch_result(la::launch_rmsnorm_rows(a, as_stream(stream)), "rmsnorm launch");
+}
+
+int la_gate_activations(const void *ab, int64_t ld, int t, int na, int nb, float *g,
+                        float *beta, uint64_t stream) {
+    if (t < 1) return fail(LA_ERR_COUNT, "gate activations of %d rows", t);
+    if (na < 1 || nb < 1) return fail(LA_ERR_ARG, "na and nb must be >= 1 (got %d, %d)", na, nb);
+    if (!ab || !g || !beta) return fail(LA_ERR_ARG, "ab, g and beta must not be NULL");
+    if (ld < (int64_t)na + nb) return fail(LA_ERR_ARG, "ld (%lld) is below na + nb", (long long)ld);
+    la::GateArgs a{ab, ld, t, na, nb, g, beta};
+    return launch_result(la::launch_gate_activations(a, as_stream(stream)), "gate activations launch");
+}
+
 }  // extern "C"

@@ -112,4 +112,26 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_bf16(const GemmArgs &a, cudaStream_t st);
 
+// Row RMSNorm y = x / sqrt(mean(x^2) + eps) * w (bf16; width a multiple of 8, at most
+// rmsnorm_rows_max_width()).
+struct RowNormArgs {
+    const void *x, *w;
+    void *y;
+    int rows, width;
+    int64_t ldx, ldy;
+    float eps;
+};
+cudaError_t launch_rmsnorm_rows(const RowNormArgs &a, cudaStream_t st);
+int rmsnorm_rows_max_width();
+
+// Gate activations: g = -softplus(a) [t][na], beta = sigmoid(b) [t][nb] (fp32) from the bf16
+// gate projection rows [t][ld] holding a | b.
+struct GateArgs {
+    const void *ab;
+    int64_t ld;
+    int t, na, nb;
+    float *g, *beta;
+};
+cudaError_t launch_gate_activations(const GateArgs &a, cudaStream_t st);
+
 }  // namespace la

@@ -20,8 +20,9 @@ import math
 import torch
 
 from . import (conv1d_silu_l2_prefill, conv1d_silu_prefill, conv1d_silu_prefill_varlen,
-               decode_step, decode_workspace_bytes, gdn_prefill_batched, gdn_prefill_varlen,
-               kda_prefill, l2norm_heads, pointer_array, prefill_front, prefill_workspace_bytes)
+               decode_step, decode_workspace_bytes, gate_activations, gdn_prefill_batched,
+               gdn_prefill_varlen, gemm_bf16, kda_prefill, l2norm_heads, pointer_array,
+               prefill_front, prefill_workspace_bytes, rmsnorm_rows)
 
 
 class PrefillPass:
@@ -136,3 +137,26 @@ class DecodeStep:
                     kda=wl.variant == "kda", l2_eps=self.eps, scale=self.scale,
                     workspace=self.workspace, stream=stream)
         return self.out
+
+
+class Phase1:
+    """Phase 1 of a layer over the stacked hidden rows ("split_prefill.rs",
+    prefill_phase1_proj_batched: norm, QKVZ, gates), through the library:
+    rmsnorm_rows -> three projection GEMMs (q|k|v, z, gate pre-activations a|b) -> gate
+    activations. Weights are the caller's ([out][in] bf16); outputs are device tensors:
+    x [t][cd] (the conv input), z [t][Hv*dv], g (fp32 [t][Hv] or [t][Hv*dk]), beta [t][Hv]."""
+
+    def __init__(self, wl, norm_w, w_qkv, w_z, w_ab, *, eps=1e-6):
+        self.wl, self.norm_w, self.w_qkv, self.w_z, self.w_ab, self.eps = (
+            wl, norm_w, w_qkv, w_z, w_ab, eps)
+        self.na = wl.Hv * (wl.d if wl.variant == "kda" else 1)
+
+    def run(self, hidden, stream=None):
+        y = rmsnorm_rows(hidden, self.norm_w, eps=self.eps, stream=stream)
+        x = gemm_bf16(y, self.w_qkv, stream=stream)
+        z = gemm_bf16(y, self.w_z, stream=stream)
+        n_ab = self.w_ab.shape[0]  # rows padded to 16 bytes (the GEMM's output stride rule)
+        ab = torch.empty(y.shape[0], (n_ab + 7) // 8 * 8, dtype=y.dtype, device=y.device)[:, :n_ab]
+        gemm_bf16(y, self.w_ab, ab, stream=stream)
+        g, beta = gate_activations(ab, self.na, stream=stream)
+        return dict(y=y, x=x, z=z, ab=ab, g=g, beta=beta)

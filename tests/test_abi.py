@@ -233,3 +233,15 @@ def test_gemm_refusals(lib):
     assert f(A, B, A * 64, 8, 8, 12, 12, 16, 8, 0) == lib.LA_ERR_ARG        # lda not 16 B
     assert f(A, B, A * 64, 8, 16, 8, 8, 8, 8, 0) == lib.LA_ERR_ARG          # ldc < N
     assert f(A, B, A + 64, 8, 8, 8, 8, 8, 8, 0) == lib.LA_ERR_ARG           # c overlaps a
+
+
+def test_phase1_elementwise_refusals(lib):
+    L = lib._load()
+    assert L.la_rmsnorm_rows(A, A * 2, A * 3, 0, 64, 64, 64, 1e-6, 0) == lib.LA_ERR_COUNT
+    assert L.la_rmsnorm_rows(A, A * 2, A * 3, 4, 60, 64, 64, 1e-6, 0) == lib.LA_ERR_UNSUPPORTED
+    assert L.la_rmsnorm_rows(A, A * 2, A * 3, 4, 8200, 8200, 8200, 1e-6, 0) == lib.LA_ERR_UNSUPPORTED
+    assert L.la_rmsnorm_rows(A + 4, A * 2, A * 3, 4, 64, 64, 64, 1e-6, 0) == lib.LA_ERR_ARG
+    assert L.la_rmsnorm_rows(A, A * 2, A * 3, 4, 64, 60, 64, 1e-6, 0) == lib.LA_ERR_ARG
+    assert L.la_gate_activations(A, 8, 0, 4, 4, A * 2, A * 3, 0) == lib.LA_ERR_COUNT
+    assert L.la_gate_activations(A, 7, 5, 4, 4, A * 2, A * 3, 0) == lib.LA_ERR_ARG
+    assert L.la_gate_activations(A, 8, 5, 4, 4, None, A * 3, 0) == lib.LA_ERR_ARG
