@@ -322,7 +322,12 @@ def main():
     lengths = inp["lengths"]
     T = sum(lengths)
     p = PrefillPass(wl, inp)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        """Evict L2 by reading a buffer twice its size: the lines it leaves are clean, so the
+        timed step that follows pays no write-back for them."""
+        torch.max(flush)
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -334,39 +339,58 @@ def main():
 
     fused = p.can_fuse  # one launch (conv + L2 + recurrence) where the tensor-core path runs
 
-    def timed_steps(split):
+    # a single stream with too few (stream, head) units to fill the GPU: the chunk-parallel scan
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    seg_s = min(8, max(1, (n_sm // wl.Hv + 1) // 2)) if (fused and wl.B == 1) else 1
+
+    def timed_steps(mode):
         """Per-step CUDA events on the launching stream, L2 flushed before each step (outside
-        the events). split: the front end and the recurrence as separate launches."""
+        the events). mode: "split" (front end, then the recurrence), "fused" (one launch),
+        "seg" (front end, then the segmented recurrence)."""
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             ev[i][0].record(stream)
-            if split:
-                p.front_end()
-            else:
+            if mode == "fused":
                 p.fused()
+            else:
+                p.front_end()
             ev[i][1].record(stream)
-            if split:
+            if mode == "split":
                 p.recurrence()
+            elif mode == "seg":
+                p.recurrence_segmented(seg_s)
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         return ([e[0].elapsed_time(e[2]) for e in ev], [e[0].elapsed_time(e[1]) for e in ev],
                 [e[1].elapsed_time(e[2]) for e in ev])
 
-    # Both public paths where both exist (two launches; one fused launch); the step is the
-    # faster of the two, decided on this run's own timings.
+    # Every public path that applies (two launches; one fused launch; for a single stream the
+    # segmented scan); the step is the fastest, decided on this run's own timings.
     clocks = ClockSampler(local)
     clocks.start()
-    split_ms, front_ms, rec_ms = timed_steps(split=True)
-    fused_ms = None
+    split_ms, front_ms, rec_ms = timed_steps("split")
+    fused_ms = seg_ms = seg_rec_ms = None
     if fused:
         for _ in range(args.warmup):
             p.fused()
         torch.cuda.synchronize()
-        fused_ms, _, _ = timed_steps(split=False)
+        fused_ms, _, _ = timed_steps("fused")
+    if seg_s > 1:
+        for _ in range(args.warmup):
+            p.front_end()
+            p.recurrence_segmented(seg_s)
+        torch.cuda.synchronize()
+        seg_ms, _, seg_rec_ms = timed_steps("seg")
     clk = clocks.stop()
-    use_fused = fused and sum(fused_ms) < sum(split_ms)
-    step_ms = fused_ms if use_fused else split_ms
+    cands = {"split": sum(split_ms)}
+    if fused_ms:
+        cands["fused"] = sum(fused_ms)
+    if seg_ms:
+        cands["seg"] = sum(seg_ms)
+    best = min(cands, key=cands.get)
+    use_fused = best == "fused"
+    step_ms = {"split": split_ms, "fused": fused_ms, "seg": seg_ms}[best]
     value, ms, _ = aggregate(T, sum(step_ms) / len(step_ms), pg, dev)
 
     # ---- end to end through the public API: pinned host inputs in, result out, every step
@@ -376,7 +400,11 @@ def main():
     out_h = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (x_h, g_h, b_h))
     d2h = out_h.numel() * out_h.element_size()
-    run = p.fused if use_fused else p.run_unfused
+    def run_seg():
+        p.front_end()
+        p.recurrence_segmented(seg_s)
+
+    run = {"fused": p.fused, "split": p.run_unfused, "seg": run_seg}[best]
     for _ in range(2):
         inp["x"].copy_(x_h, non_blocking=True)
         run()
@@ -413,15 +441,17 @@ def main():
     B_alg, F_alg = path_algorithmic(wl, lengths)
     # dominant kernel: the fused layer kernel (its events also bracket the one-block stream
     # order kernel launched before it), else the recurrence of the two-launch path
-    dom_bytes, dom_ms = (B_alg, fused_avg) if use_fused else (kb["recurrence"], rec_avg)
+    seg_rec_avg = sum(seg_rec_ms) / len(seg_rec_ms) if seg_rec_ms else None
+    dom_bytes, dom_ms = ((B_alg, fused_avg) if use_fused else
+                         (kb["recurrence"], seg_rec_avg if best == "seg" else rec_avg))
     dom_achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     t_roof = max(F_alg / (float(peaks["bf16_tflops"]) * 1e12), B_alg / (hbm * 1e9))
     tc = uses_tensor_cores(wl)
     kernel_file = "chunk_tc.cu" if tc else "chunk_simt.cu"
     kernel_name = "chunk_tc_kernel" if tc else "chunk_simt_kernel"
-    traffic = profiled_traffic(kernel_file, wl.name, "fused" if use_fused else "split")
+    traffic = profiled_traffic(kernel_file, wl.name, best)
     # fused: stream order + layer kernel; else conv(+L2), (stream order), recurrence
-    launches_per_step = 2 if use_fused else (3 if tc else 2)
+    launches_per_step = 2 if use_fused else (6 if best == "seg" else (3 if tc else 2))
     line = {
         "metric": METRIC,
         "value": value,
@@ -438,12 +468,14 @@ def main():
                 "g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
         "config": {"workload": wl.name, "streams": wl.B, "tokens_per_step": T,
                    "path": ("one fused launch (la_prefill_front)" if use_fused else
+                            f"fused conv1d+SiLU+L2, then the segmented recurrence ({seg_s} "
+                            "segments, la_prefill_segmented)" if best == "seg" else
                             "two launches (fused conv1d+SiLU+L2, then the recurrence)"),
                    "Hk": wl.Hk, "Hv": wl.Hv, "head_dim": wl.d, "variant": wl.variant,
                    "activations": wl.dtype, "states": "f32", "chunk": CHUNK,
                    "compute": ("tensor cores: bf16 (raw inputs) and tf32 (state-derived) MMAs, "
                                "fp32 accumulate; CUDA cores fp32" if tc else "CUDA cores fp32"),
-                   "l2": "flushed between timed steps (write of a 258 MiB buffer)",
+                   "l2": "flushed between timed steps (read of a 258 MiB buffer, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -451,7 +483,10 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": {"bound": "hbm",
                      "kernel": kernel_name + (" (conv1d+SiLU+L2+recurrence, one launch)"
-                                              if use_fused else " (recurrence)"),
+                                              if use_fused else
+                                              f" (segmented recurrence, {seg_s} segments: setup, "
+                                              "recurrence, join, correction launches)"
+                                              if best == "seg" else " (recurrence)"),
                      "achieved": dom_achieved, "peak": hbm, "unit": "GB/s",
                      "frac": dom_achieved / hbm, "traffic": traffic,
                      "peak_source": f"{peak_src} hbm_gbs",
@@ -459,7 +494,10 @@ def main():
                      "avg_launch_ms": dom_ms},
         "phases_ms": {"two launches": split_avg, "front_end(conv1d+silu, l2)": front_avg,
                       "recurrence": rec_avg,
-                      **({"one fused launch (la_prefill_front)": fused_avg} if fused else {})},
+                      **({"one fused launch (la_prefill_front)": fused_avg} if fused else {}),
+                      **({f"front end + segmented recurrence ({seg_s} segments)":
+                          sum(seg_ms) / len(seg_ms),
+                          "segmented recurrence": seg_rec_avg} if seg_ms else {})},
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "frac": t_roof / (ms * 1e-3),
                           "bytes_alg": B_alg, "flops_alg": F_alg,
                           "peaks": f"{peak_src}: {hbm} GB/s, {peaks['bf16_tflops']} TFLOP/s bf16"},
@@ -483,7 +521,12 @@ def run_proj(args, wl, dev, local, rank, world, pg):
     a = torch.randn(T, Kd, generator=gen, device=dev).to(torch.bfloat16)
     w = (torch.randn(N, Kd, generator=gen, device=dev) / math.sqrt(Kd)).to(torch.bfloat16)
     c = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        """Evict L2 by reading a buffer twice its size: the lines it leaves are clean, so the
+        timed step that follows pays no write-back for them."""
+        torch.max(flush)
     stream = torch.cuda.current_stream()
 
     def timed(fn):
@@ -492,7 +535,7 @@ def run_proj(args, wl, dev, local, rank, world, pg):
         torch.cuda.synchronize()
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            flush_l2()
             ev[i][0].record(stream)
             fn()
             ev[i][1].record(stream)
@@ -540,7 +583,7 @@ def run_proj(args, wl, dev, local, rank, world, pg):
         "data": "synthetic (seeded; hidden rows ~N(0,1), weights ~N(0,1/hidden))",
         "config": {"workload": wl.name, "tokens_per_step": T, "hidden": Kd, "outputs": N,
                    "path": "la_gemm_bf16 (tcgen05 + TMA, 128x256 tiles, fp32 accumulation)",
-                   "l2": "flushed between timed steps (write of a 258 MiB buffer)",
+                   "l2": "flushed between timed steps (read of a 258 MiB buffer, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gpu_launches": args.steps,
         "clocks": clk,
@@ -566,7 +609,12 @@ def run_decode(args, wl, inp, dev, local, rank, world, pg):
     from linear_attention_chunked_conv1d_gb300.path import DecodeStep
 
     p = DecodeStep(wl, inp)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        """Evict L2 by reading a buffer twice its size: the lines it leaves are clean, so the
+        timed step that follows pays no write-back for them."""
+        torch.max(flush)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         p.run()
@@ -578,7 +626,7 @@ def run_decode(args, wl, inp, dev, local, rank, world, pg):
     clocks.start()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[i][0].record(stream)
         p.run()
         ev[i][1].record(stream)
@@ -634,7 +682,7 @@ def run_decode(args, wl, inp, dev, local, rank, world, pg):
                    "activations": wl.dtype, "states": "f32",
                    "path": "la_decode_step (conv1d+SiLU+L2 launch, recurrence launch)",
                    "compute": "CUDA cores fp32 (matrix-vector work per state)",
-                   "l2": "flushed between timed steps (write of a 258 MiB buffer); the h states "
+                   "l2": "flushed between timed steps (read of a 258 MiB buffer, outside the events); the h states "
                          f"({wl.B * wl.Hv * wl.d * wl.d * 4 >> 20} MiB) exceed L2 as well",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gpu_launches": 2 * args.steps,

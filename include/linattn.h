@@ -305,6 +305,24 @@ int la_rmsnorm_rows(const void *x, const void *w, void *y, int rows, int width, 
 int la_gate_activations(const void *ab, int64_t ld, int t, int na, int nb, float *g,
                         float *beta, uint64_t stream);
 
+/* Chunk-parallel prefill of ONE long stream: the recurrence (GDN, kda == 0, or KDA, kda == 1;
+ * q, k, v, g, beta, out as for la_gdn_prefill_varlen / la_kda_prefill with B = 1) with the
+ * stream cut into `segments` pieces (at multiples of 64 tokens, at most 8) that run side by
+ * side on the tensor cores and are then joined through each piece's state transition
+ * (H_end = M H_0 + N; o_t = o_t(0) + H_0^T p_t). Not on the pages (their chunk_scan walks a
+ * head's chunks in one block): it is for calls with too few (stream, v-head) units to fill the
+ * GPU. Worth it while Hv * (2 * segments - 1) stays within the SM count. segments = 1 is the
+ * plain call. Covers bf16 with dk = dv = 128 (else LA_ERR_UNSUPPORTED).
+ * workspace  at least la_prefill_segmented_workspace_bytes(total_tokens, Hv, segments) bytes.
+ * Count rule: 1 <= total_tokens <= max_tokens. */
+size_t la_prefill_segmented_workspace_bytes(int total_tokens, int Hv, int segments);
+int la_prefill_segmented(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                         const void *v, const float *g, const float *beta, void *out,
+                         int total_tokens, int max_tokens, int Hk, int Hv, int dk, int dv,
+                         int64_t q_stride, int64_t k_stride, int64_t v_stride, float scale,
+                         int kda, int segments, int dtype, void *workspace,
+                         size_t workspace_bytes, uint64_t stream);
+
 #ifdef __cplusplus
 }
 #endif

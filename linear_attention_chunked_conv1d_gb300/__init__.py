@@ -72,6 +72,10 @@ _SIGS = {
                           _i32, _i32, _vp, _sz, _u64], ctypes.c_int),
     "la_gated_rmsnorm": ([_vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _i32, _u64], ctypes.c_int),
     "la_gemm_bf16": ([_vp, _vp, _vp, _i32, _i32, _i32, _i64, _i64, _i64, _u64], ctypes.c_int),
+    "la_prefill_segmented_workspace_bytes": ([_i32, _i32, _i32], _sz),
+    "la_prefill_segmented": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+                              _i32, _i64, _i64, _i64, _f32, _i32, _i32, _i32, _vp, _sz, _u64],
+                             ctypes.c_int),
     "la_rmsnorm_rows": ([_vp, _vp, _vp, _i32, _i32, _i64, _i64, _f32, _u64], ctypes.c_int),
     "la_gate_activations": ([_vp, _i64, _i32, _i32, _i32, _vp, _vp, _u64], ctypes.c_int),
     "la_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32], _sz),
@@ -350,3 +354,22 @@ def gate_activations(ab, na, g=None, beta=None, *, stream=None):
     _check(_load().la_gate_activations(_ptr(ab), _row_stride(ab), t, na, nb, _ptr(g), _ptr(beta),
                                        _stream(stream)))
     return g, beta
+
+
+def prefill_segmented_workspace_bytes(total_tokens, Hv, segments) -> int:
+    return int(_load().la_prefill_segmented_workspace_bytes(total_tokens, Hv, segments))
+
+
+def prefill_segmented(h_state_ptrs, q, k, v, gate, beta, out, *, Hk, Hv, dk, dv, kda, segments,
+                      total_tokens=None, scale=None, max_tokens=None, workspace=None,
+                      stream=None) -> None:
+    """The recurrence of ONE long stream with its tokens cut into `segments` pieces that run
+    side by side on the tensor cores, then joined (chunk-parallel scan)."""
+    total = q.shape[0] if total_tokens is None else total_tokens
+    scale = 1.0 / math.sqrt(dk) if scale is None else scale
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_load().la_prefill_segmented(
+        _ptr(h_state_ptrs), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta), _ptr(out), total,
+        max_tokens if max_tokens is not None else total, Hk, Hv, dk, dv, _row_stride(q),
+        _row_stride(k), _row_stride(v), float(scale), 1 if kda else 0, int(segments),
+        _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))

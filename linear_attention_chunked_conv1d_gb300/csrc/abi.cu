@@ -562,4 +562,39 @@ int la_gate_activations(const void *ab, int64_t ld, int t, int na, int nb, float
     return launch_result(la::launch_gate_activations(a, as_stream(stream)), "gate activations launch");
 }
 
+size_t la_prefill_segmented_workspace_bytes(int total_tokens, int Hv, int segments) {
+    if (total_tokens < 1 || Hv < 1) return 0;
+    return la::segmented_workspace_bytes(total_tokens, Hv, segments);
+}
+
+int la_prefill_segmented(const uint64_t *h_state_ptrs, const void *q, const void *k,
+                         const void *v, const float *g, const float *beta, void *out,
+                         int total_tokens, int max_tokens, int Hk, int Hv, int dk, int dv,
+                         int64_t q_stride, int64_t k_stride, int64_t v_stride, float scale,
+                         int kda, int segments, int dtype, void *workspace,
+                         size_t workspace_bytes, uint64_t stream) {
+    if (total_tokens <= 0 || total_tokens > max_tokens)
+        return fail(LA_ERR_COUNT, "prefill of %d tokens does not fit max_tokens %d", total_tokens,
+                    max_tokens);
+    if (kda != 0 && kda != 1) return fail(LA_ERR_ARG, "kda must be 0 (GDN) or 1 (KDA)");
+    if (segments < 1 || segments > la::kMaxSegments)
+        return fail(LA_ERR_ARG, "segments %d outside 1..%d", segments, la::kMaxSegments);
+    LA_TRY(check_dtype(dtype));
+    if (!uses_tensor_cores(dtype, dk, dv))
+        return fail(LA_ERR_UNSUPPORTED, "the segmented scan covers bf16 with dk = dv = 128");
+    const size_t need = la_prefill_segmented_workspace_bytes(total_tokens, Hv, segments);
+    LA_TRY(rec_common(h_state_ptrs, q, k, v, g, beta, out, 1, Hk, Hv, dk, dv, q_stride, k_stride,
+                      v_stride, dtype, workspace, workspace_bytes, need));
+    la::RecArgs a{};
+    a.h_ptrs = h_state_ptrs; a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
+    a.cu = nullptr; a.B = 1; a.T_each = total_tokens; a.total = total_tokens;
+    a.max_seqlen = total_tokens;
+    a.Hk = Hk; a.Hv = Hv; a.dk = dk; a.dv = dv;
+    a.q_stride = q_stride; a.k_stride = k_stride; a.v_stride = v_stride;
+    a.scale = scale; a.pad_fill = 0.f; a.dtype = dtype; a.kda = kda == 1;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.status = status_ptr();
+    return launch_result(la::launch_segmented(a, segments, as_stream(stream)), "segmented scan launch");
+}
+
 }  // extern "C"

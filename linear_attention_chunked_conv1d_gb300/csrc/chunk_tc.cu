@@ -155,8 +155,10 @@ __device__ __forceinline__ void load_kq(const RecArgs &a, unsigned char *sm, int
     }
 }
 __device__ __forceinline__ void load_v(const RecArgs &a, unsigned char *sm, int tok0, int n,
-                                       int j, int tid) {
-    const __nv_bfloat16 *vp = reinterpret_cast<const __nv_bfloat16 *>(a.v) + (int64_t)j * TC_D;
+                                       int j, int tid, bool alt) {
+    const __nv_bfloat16 *vp =
+        reinterpret_cast<const __nv_bfloat16 *>(alt ? a.v_alt : a.v) + (int64_t)j * TC_D;
+    const int64_t vs = alt ? 0 : a.v_stride;
     const uint32_t base = tc::smem_u32(sm + SM_V);
 #pragma unroll
     for (int m = 0; m < 1024 / TC_THREADS; ++m) {
@@ -165,7 +167,7 @@ __device__ __forceinline__ void load_v(const RecArgs &a, unsigned char *sm, int 
         const bool valid = row < n;
         const int srow = tok0 + (valid ? row : 0);
         cp_async16(base + tc::sw128_offset(row, ch * 8, 64, 2),
-                   vp + (int64_t)srow * a.v_stride + ch * 8, valid);
+                   vp + (int64_t)srow * vs + ch * 8, valid);
     }
 }
 
@@ -438,12 +440,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         const int s = P.perm[u / Hv];
         const int j = u % Hv;
         const int kh = j / group;
+        const bool alt = a.use_alt && s >= a.alt_from;  // segmented scan: a transition run
         int t0, len;
-        if (!stream_range(a.cu, s, a.T_each, a.total, a.max_seqlen, a.status, t0, len)) continue;
+        if (!(alt ? stream_range(a.cu_alt, s - a.alt_from, 0, a.total, a.max_seqlen, a.status, t0, len)
+                  : stream_range(a.cu, s, a.T_each, a.total, a.max_seqlen, a.status, t0, len)))
+            continue;
         if (len <= 0) continue;
         const int nch = (len + TC_C - 1) / TC_C;
         float *hg = reinterpret_cast<float *>(a.h_ptrs[s]) + (int64_t)j * TC_D * TC_D;
-        __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(a.out) + (int64_t)j * TC_D;
+        __nv_bfloat16 *og = reinterpret_cast<__nv_bfloat16 *>(alt ? a.out_alt : a.out) + (int64_t)j * TC_D;
 
         __nv_bfloat16 *conv_state =
             FRONT && a.conv_k > 1 ? reinterpret_cast<__nv_bfloat16 *>(a.conv_state_ptrs[s]) : nullptr;
@@ -452,7 +457,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             load_raw(a, sm, conv_state, t0, len, 0, kh, j, tid);
         } else {
             load_kq(a, sm, t0, min(TC_C, len), kh, tid);
-            load_v(a, sm, t0, min(TC_C, len), j, tid);
+            load_v(a, sm, t0, min(TC_C, len), j, tid, alt);
         }
         cp_async_commit();
         // S[d][c] = H[c][d]: thread (d, part) loads columns c in [D32*part, D32*part + D32)
@@ -907,7 +912,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             if (!last) {  // V tile consumed by the identity MMA: next chunk's V (FRONT: the
                           // raw rows, into the tf32 K|Q buffer the state MMA has read) in flight
                 if (FRONT) load_raw(a, sm, nullptr, t0, len, (ch + 1) * TC_C, kh, j, tid);
-                else load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid);
+                else load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid, alt);
                 cp_async_commit();
             }
             {

@@ -19,8 +19,6 @@
 // stores are guarded.
 #include <cuda.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -197,41 +195,6 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     if (*err && threadIdx.x == 0) raise_status(status, LA_DEV_TIMEOUT);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no libcuda link).
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// 2-D bf16 map of a row-major [rows][cols] matrix (row stride ld elements), boxes of
-// box_rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t ld,
-              uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)GK, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int device_sms() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -243,7 +206,8 @@ int device_sms() {
 
 cudaError_t launch_gemm_bf16(const GemmArgs &a, cudaStream_t st) {
     CUtensorMap ma, mw;
-    if (!make_map(&ma, a.a, a.M, a.K, a.lda, GM) || !make_map(&mw, a.w, a.N, a.K, a.ldw, GN))
+    if (!make_map_bf16_2d(&ma, a.a, a.M, a.K, a.lda, GK, GM, true) ||
+        !make_map_bf16_2d(&mw, a.w, a.N, a.K, a.ldw, GK, GN, true))
         return cudaErrorInvalidValue;
     const int64_t ntiles = (int64_t)((a.M + GM - 1) / GM) * ((a.N + GN - 1) / GN);
     const int grid = (int)(ntiles < device_sms() ? ntiles : device_sms());

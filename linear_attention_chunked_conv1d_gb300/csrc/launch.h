@@ -57,6 +57,14 @@ struct RecArgs {
     int64_t x_stride;
     int conv_k;
     float l2_eps;
+    // Segmented scan (tensor-core kernel, not with the fused front end): streams s >= alt_from
+    // read v as zero (v_alt: one zero row, stride 0) and write their outputs to out_alt.
+    // Their token ranges come from cu_alt (index s - alt_from).
+    bool use_alt;
+    int alt_from;
+    const int32_t *cu_alt;
+    const void *v_alt;
+    void *out_alt;
     // Gated RMSNorm in the output store (tensor-core kernel only): when z is set, out receives
     // o / sqrt(mean(o^2) + norm_eps) * norm_w * SiLU(z) per (token, v-head) row, from the bf16 o.
     const void *z, *norm_w;
@@ -133,5 +141,19 @@ struct GateArgs {
     float *g, *beta;
 };
 cudaError_t launch_gate_activations(const GateArgs &a, cudaStream_t st);
+
+// Chunk-parallel scan of one long stream (tensor-core path): the stream's tokens cut into up to
+// kMaxSegments segments run side by side, then joined (segscan.cu). `a` describes one stream
+// (cu == nullptr, B == 1); its workspace must hold segmented_workspace_bytes(...).
+constexpr int kMaxSegments = 8;
+int segmented_plan_segments(int total, int requested);
+size_t segmented_workspace_bytes(int total, int Hv, int segments);
+cudaError_t launch_segmented(const RecArgs &a, int segments, cudaStream_t st);
+
+// Encodes a 2-D tiled TMA map (a CUtensorMap, 64-byte aligned storage of 128 bytes) of a
+// row-major bf16 matrix [rows][cols] with row stride ld elements, boxes of box_rows x box_cols,
+// optional 128-byte swizzle; out-of-range elements of a box read as zero. False on failure.
+bool make_map_bf16_2d(void *map, const void *base, int64_t rows, int64_t cols, int64_t ld,
+                      uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 }  // namespace la

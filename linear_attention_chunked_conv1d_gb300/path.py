@@ -22,7 +22,8 @@ import torch
 from . import (conv1d_silu_l2_prefill, conv1d_silu_prefill, conv1d_silu_prefill_varlen,
                decode_step, decode_workspace_bytes, gate_activations, gdn_prefill_batched,
                gdn_prefill_varlen, gemm_bf16, kda_prefill, l2norm_heads, pointer_array,
-               prefill_front, prefill_workspace_bytes, rmsnorm_rows)
+               prefill_front, prefill_segmented, prefill_segmented_workspace_bytes,
+               prefill_workspace_bytes, rmsnorm_rows)
 
 
 class PrefillPass:
@@ -89,6 +90,18 @@ class PrefillPass:
         else:
             gdn_prefill_varlen(self.h_ptrs, self.q, self.k, self.v, inp["g"], inp["beta"],
                                self.out, inp["cu_seqlens"], max_seqlen=self.max_seqlen, **common)
+
+    def recurrence_segmented(self, segments, stream=None):
+        """The recurrence of a single stream as a chunk-parallel scan (la_prefill_segmented)."""
+        wl, inp = self.wl, self.inp
+        assert wl.B == 1, "the segmented scan covers one stream"
+        nbytes = prefill_segmented_workspace_bytes(self.T, wl.Hv, segments)
+        if getattr(self, "_seg_ws", None) is None or self._seg_ws.numel() < nbytes:
+            self._seg_ws = torch.empty(nbytes, dtype=torch.uint8, device=self.out.device)
+        prefill_segmented(self.h_ptrs, self.q, self.k, self.v, inp["g"], inp["beta"], self.out,
+                          Hk=wl.Hk, Hv=wl.Hv, dk=wl.d, dv=wl.d, kda=wl.variant == "kda",
+                          segments=segments, scale=self.scale, workspace=self._seg_ws,
+                          stream=stream)
 
     def fused(self, stream=None):
         """conv1d + SiLU + L2 + recurrence in one launch (bf16, head dim 128)."""

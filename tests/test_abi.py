@@ -245,3 +245,22 @@ def test_phase1_elementwise_refusals(lib):
     assert L.la_gate_activations(A, 8, 0, 4, 4, A * 2, A * 3, 0) == lib.LA_ERR_COUNT
     assert L.la_gate_activations(A, 7, 5, 4, 4, A * 2, A * 3, 0) == lib.LA_ERR_ARG
     assert L.la_gate_activations(A, 8, 5, 4, 4, None, A * 3, 0) == lib.LA_ERR_ARG
+
+
+def test_segmented_refusals(lib):
+    L = lib._load()
+    args = lambda **kw: dict(dict(total=100, maxt=200, Hk=1, Hv=2, dk=128, dv=128, kda=0, S=2,
+                                  dtype=1, ws=A * 64, wsb=1 << 30), **kw)  # noqa: E731
+
+    def rc(**kw):
+        a = args(**kw)
+        return L.la_prefill_segmented(A, A, A, A, A, A, A * 2, a["total"], a["maxt"], a["Hk"],
+                                      a["Hv"], a["dk"], a["dv"], 256, 256, 256, 0.1, a["kda"],
+                                      a["S"], a["dtype"], a["ws"], a["wsb"], 0)
+    assert rc(total=0) == lib.LA_ERR_COUNT
+    assert rc(total=300) == lib.LA_ERR_COUNT
+    assert rc(S=0) == lib.LA_ERR_ARG and rc(S=9) == lib.LA_ERR_ARG
+    assert rc(dtype=0) == lib.LA_ERR_UNSUPPORTED
+    assert rc(dk=64, dv=64) == lib.LA_ERR_UNSUPPORTED
+    assert rc(wsb=100) == lib.LA_ERR_ARG
+    assert L.la_prefill_segmented_workspace_bytes(4096, 32, 2) > 32 * 128 * 128 * 4 * 3
