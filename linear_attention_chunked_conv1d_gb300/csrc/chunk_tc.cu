@@ -374,6 +374,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     float *atp = reinterpret_cast<float *>(sm + SM_AT);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_BARS);
     uint64_t *bar_b = bar_a + 1;
+    uint64_t *bar_c = reinterpret_cast<uint64_t *>(sm + SM_BARS + 40);  // state update done
     volatile int *err = reinterpret_cast<volatile int *>(sm + SM_BARS + 16);
     volatile int *unit_sh = err + 1;
     volatile int *slow_sh = err + 2;
@@ -393,6 +394,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         *err = 0;
         tc::mbar_init(bar_a, 1);
         tc::mbar_init(bar_b, 1);
+        tc::mbar_init(bar_c, 1);
         tc::fence_mbar_init();
     }
     // identity tile (bf16, K-major 64x64) for the transposing MMAs
@@ -411,13 +413,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     tc::fence_after_sync();
     const uint32_t tm = *tmem_sh;
     const uint32_t sb = tc::smem_u32(sm);  // shared-window address of the tile area (uniform)
-    uint32_t phase_a = 0, phase_b = 0;
+    uint32_t phase_a = 0, phase_b = 0, phase_c = 0;
+    bool pend_c = false;  // a state-update MMA group not yet waited for
 
     auto wait_bar = [&](uint64_t *bar, uint32_t &ph) {
         const bool ok = tc::mbar_wait(bar, ph, WAIT_NS);
         ph ^= 1u;
         if (!ok) *err = 1;
         tc::fence_after_sync();
+    };
+    // The state update of a chunk completes on bar_c, after the output MMA (bar_b): the output
+    // epilogue and the next chunk's prologue run meanwhile. Wait for it before anything reads S
+    // or rewrites the operands it reads (the transposed key tile, the U' columns).
+    auto wait_state = [&]() {
+        if (pend_c) {
+            wait_bar(bar_c, phase_c);
+            pend_c = false;
+        }
     };
 
     ColWalk w_kq, w_kqg, w_kr;
@@ -624,6 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
             // ---------------- D1 = [K;Q] K^T (KDA: decays split at row 31); GDN also K^T
             bool slow = false;
+            if (KDA) wait_state();  // the Kr tile below is the previous state update's operand
             if (KDA) {
                 const int c = row;
                 const float gm = sf[SF_GM + c];
@@ -724,6 +737,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 
             if (!KDA) {  // GDN: stage while D1 and K^T are computed, then start the state MMA
                 stage_state_operands();
+                wait_state();
                 issue_mma2();
             }
 
@@ -1034,14 +1048,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     const uint64_t bp = tc::sdesc_sw128((sb + SM_P) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
                     tc::mma_tf32_ts(tm + COL_D4, tm + COL_RU + kk * 8, bp, id64, kk > 0);
                 }
+                tc::mma_commit(bar_b);  // the output MMA: the epilogue may start
                 const uint32_t a5 = KDA ? COL_RU : COL_RUD;
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
                     const uint64_t bk = tc::sdesc_sw128((sb + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
                     tc::mma_tf32_ts(tm + COL_S, tm + a5 + kk * 8, bk, id128, 1);
                 }
-                tc::mma_commit(bar_b);
+                tc::mma_commit(bar_c);
             }
+            pend_c = true;
             if (FRONT && !last) {  // next chunk's q, k, v tiles while the tensor core works
                 conv_tile_any(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane);
                 tc::fence_async_smem();
@@ -1077,6 +1093,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             pend_n = 0;
         }
 
+        wait_state();
+        if (*err) break;
         // state back: H[c][d] = S[d][c]
 #pragma unroll
         for (int g = 0; g < D32 / 16; ++g) {
@@ -1092,6 +1110,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     }
 
     cp_async_wait_all();
+    if (pend_c) tc::mbar_wait(bar_c, phase_c, WAIT_NS);  // after an error: no MMA left in flight
     if (*err && tid == 0) raise_status(a.status, LA_DEV_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
