@@ -173,3 +173,67 @@ class Phase1:
         gemm_bf16(y, self.w_ab, ab, stream=stream)
         g, beta = gate_activations(ab, self.na, stream=stream)
         return dict(y=y, x=x, z=z, ab=ab, g=g, beta=beta)
+
+
+class StreamedPrefill:
+    """Prefill steps fed from pinned host memory and read back to it, pipelined over three
+    streams: the host->device copy of step i+1 and the device->host copy of step i-1 overlap
+    the compute of step i. Two sets of device inputs and outputs alternate; the carried conv and
+    h states are shared and advance in step order on the compute stream.
+
+    `mode`: "split" (fused conv+L2, then the recurrence), "fused" (la_prefill_front) or "seg"
+    (fused conv+L2, then the segmented recurrence with `segments` pieces, one stream)."""
+
+    def __init__(self, wl, inputs: dict, *, mode="split", segments=1, compute_stream=None):
+        self.mode, self.segments = mode, segments
+        dev = inputs["x"].device
+        self.passes = []
+        for _ in range(2):
+            inp = dict(inputs)
+            for name in ("x", "g", "beta"):
+                inp[name] = torch.empty_like(inputs[name])
+            self.passes.append(PrefillPass(wl, inp))
+        self.compute = compute_stream or torch.cuda.current_stream(dev)
+        self.copy_in = torch.cuda.Stream(dev)
+        self.copy_out = torch.cuda.Stream(dev)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.drained = [torch.cuda.Event() for _ in range(2)]
+
+    def _run(self, p):
+        if self.mode == "fused":
+            p.fused(self.compute)
+        elif self.mode == "seg":
+            p.front_end(self.compute)
+            p.recurrence_segmented(self.segments, self.compute)
+        else:
+            p.run_unfused(self.compute)
+
+    def step(self, i, x_h, g_h, beta_h, out_h):
+        """Step i: inputs from the pinned host tensors, the output into out_h (all queued)."""
+        b = i % 2
+        p = self.passes[b]
+        with torch.cuda.stream(self.copy_in):
+            self.copy_in.wait_event(self.computed[b])  # step i-2 is done with these inputs
+            p.inp["x"].copy_(x_h, non_blocking=True)
+            p.inp["g"].copy_(g_h, non_blocking=True)
+            p.inp["beta"].copy_(beta_h, non_blocking=True)
+            self.copied[b].record(self.copy_in)
+        self.compute.wait_event(self.copied[b])
+        self.compute.wait_event(self.drained[b])  # step i-2's output has been read back
+        self._run(p)
+        self.computed[b].record(self.compute)
+        with torch.cuda.stream(self.copy_out):
+            self.copy_out.wait_event(self.computed[b])
+            out_h.copy_(p.out, non_blocking=True)
+            self.drained[b].record(self.copy_out)
+
+    def start(self, event):
+        """Make every stream of the pipeline start after `event` (recorded by the caller)."""
+        for st in (self.compute, self.copy_in, self.copy_out):
+            st.wait_event(event)
+
+    def finish(self):
+        """Make the compute stream wait for the last copies back (then record on it)."""
+        self.compute.wait_event(self.drained[0])
+        self.compute.wait_event(self.drained[1])
