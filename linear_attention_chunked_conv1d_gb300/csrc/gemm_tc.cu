@@ -13,7 +13,8 @@
 //    stage) into one of two 256-column TMEM accumulators, frees each stage with tcgen05.commit;
 //  - warps 2-5: the epilogue (one TMEM lane quadrant each) drains the other accumulator to bf16
 //    while the next tile accumulates.
-// Tiles are walked m-fastest, so the blocks of one wave share the same W tiles in L2. Every
+// Tiles are walked n-fastest: a wave covers a few 128-row bands of A against all of W, so W
+// stays in L2 and A is read from HBM about once. Every
 // wait is bounded (2 s): on timeout the block records LA_DEV_TIMEOUT, stops issuing, drains its
 // own copies and MMAs, frees TMEM and returns. Tails in M, N and K come from TMA's zero fill;
 // stores are guarded.
@@ -100,7 +101,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         if (tc::elect_one()) {  // ---- TMA producer
             uint32_t it = 0;  // copies issued so far
             for (int tile = blockIdx.x; tile < ntiles && !*err; tile += gridDim.x) {
-                const int m0 = (tile % mt) * GM, n0 = (tile / mt) * GN;
+                const int m0 = (tile / nt) * GM, n0 = (tile % nt) * GN;
                 for (int k = 0; k < kb; ++k, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     if (!tc::mbar_wait(empty + s, ph ^ 1u, G_WAIT_NS) || *err) {
@@ -166,7 +167,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 break;
             }
             tc::fence_after_sync();
-            const int m0 = (tile % mt) * GM, n0 = (tile / mt) * GN;
+            const int m0 = (tile / nt) * GM, n0 = (tile % nt) * GN;
             const int row = m0 + 32 * (int)q + lane;
             __nv_bfloat16 *crow = C + (int64_t)row * ldc + n0;
 #pragma unroll 1
