@@ -223,9 +223,46 @@ def cpu_baseline(wl, inp, budget_s=12.0):
                       f"fp64 conv1d+SiLU -> L2 -> token-by-token recurrence, {elapsed:.1f} s"}
 
 
+def run_reference_proj(args, wl):
+    """Reference arm of the projection workload: the oracle's fp64 product over a sample of the
+    stacked rows (256 per step) against the full weight, timed on the host cores."""
+    import oracle
+    Kd, N = wl.hidden, 4 * wl.Hv * wl.d
+    gen = torch.Generator("cpu")
+    gen.manual_seed(0)
+    rows = 256
+    a = torch.randn(rows, Kd, generator=gen).to(torch.bfloat16)
+    w = (torch.randn(N, Kd, generator=gen) / math.sqrt(Kd)).to(torch.bfloat16)
+    af, wf = a.to(torch.float64).numpy(), w.to(torch.float64).numpy()
+    for _ in range(args.warmup):
+        oracle.linear(af, wf)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.linear(af, wf)
+    total = time.perf_counter() - t0
+    value = rows * args.steps / total
+    threads = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": PROJ_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe in DESIGN.md)",
+        "config": {"workload": wl.name, "hidden": Kd, "outputs": N},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {rows} of the stacked rows against the full "
+                                   f"{N} x {Kd} weight, fp64 matrix product"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
+        return
+    if wl.mode == "proj":
+        run_reference_proj(args, wl)
         return
     import oracle
     oracle.build()

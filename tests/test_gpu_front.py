@@ -199,3 +199,19 @@ def test_front_refusals_leave_buffers_untouched(cuda):
     torch.cuda.synchronize()
     assert torch.all(out.cpu() == 5.0)
     assert torch.equal(h.cpu(), c["h"]) and torch.equal(st.cpu(), c["st"])
+
+
+def test_front_many_short_streams(cuda):
+    """2500 streams (many empty or shorter than the conv window, a few several chunks long):
+    the stream order kernel past 1024 streams, the persistent scheduler over 5000 units, the
+    conv-state reader counts of 2500 (stream, k-head) pairs."""
+    g = torch.Generator("cpu")
+    g.manual_seed(77)
+    lengths = torch.randint(0, 6, (2500,), generator=g).tolist()
+    for i in (5, 900, 2400):
+        lengths[i] = 150 + i % 50
+    c = make_case(lengths, 1, 2, 4, False, seed=78)
+    fo, fh, fs = run_fused(cuda, c)
+    so, sh, ss = run_separate(cuda, c)
+    assert torch.equal(fo, so) and torch.equal(fh, sh) and torch.equal(fs, ss)
+    check_oracle(c, fo, fh, fs)
