@@ -8,9 +8,11 @@
 //   - segment j >= 1 runs twice in the same launch: from H_0 = 0 with the real v (outputs
 //     o_t(0) into `out`, end state N_j), and from H_0 = I with v = 0 (outputs p_t into a
 //     workspace, end state M_j);
-//   - a join kernel walks the segments: H_start(j+1) = M_j H_start(j) + N_j (H_start(1) = the end
-//     state of segment 0), ending with the stream's final state;
-//   - a correction kernel adds H_start(j)^T p_t to the outputs of segment j.
+//   - then, for j = 1 .. S-1, one launch whose blocks do two independent things from
+//     H_start(j): join blocks compute H_start(j+1) = M_j H_start(j) + N_j (the last one is the
+//     stream's final state), correction blocks add H_start(j)^T p_t to the outputs of segment j.
+//     Segment 0 runs on a copy of the true state, so the caller's state is written only by
+//     the last join.
 // This is not on the pages (they walk the chunks of a head in one block); it costs the
 // transition runs (about 2x the work for segments >= 1) and wins when a call has too few
 // (stream, v-head) units to fill the GPU, as a single long stream does.
@@ -31,14 +33,14 @@ struct SegPlan {
 // Pseudo-stream tables and the initial states of the segment runs.
 __global__ void seg_setup_kernel(SegPlan plan, int Hv, const uint64_t *h_real, int32_t *cu_p,
                                  int32_t *cu_alt, uint64_t *ptrs, float *Nb, float *Mb,
-                                 __nv_bfloat16 *zero_v) {
+                                 float *Hs, __nv_bfloat16 *zero_v) {
     const int S = plan.S, P = 2 * S - 1;
     const int64_t per = (int64_t)Hv * SD * SD;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         for (int i = 0; i <= S; ++i) cu_p[i] = plan.b[i];
         for (int i = S + 1; i <= P; ++i) cu_p[i] = plan.b[S];  // transition runs: see cu_alt
         for (int i = 0; i < S; ++i) cu_alt[i] = plan.b[i + 1];
-        ptrs[0] = h_real[0];
+        ptrs[0] = reinterpret_cast<uint64_t>(Hs);  // segment 0 runs on a copy of the state
         for (int j = 1; j < S; ++j) {
             ptrs[j] = reinterpret_cast<uint64_t>(Nb + (j - 1) * per);
             ptrs[S + j - 1] = reinterpret_cast<uint64_t>(Mb + (j - 1) * per);
@@ -53,93 +55,96 @@ __global__ void seg_setup_kernel(SegPlan plan, int Hv, const uint64_t *h_real, i
     }
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < Hv * SD; i += gridDim.x * blockDim.x)
         zero_v[i] = __float2bfloat16_rn(0.f);
+    const float4 *src = reinterpret_cast<const float4 *>(h_real[0]);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per / 4;
+         i += (int64_t)gridDim.x * blockDim.x)
+        reinterpret_cast<float4 *>(Hs)[i] = src[i];
 }
 
-constexpr int MT_LD = SD + 4;  // padded row of the transposed transition in shared memory
-constexpr size_t JOIN_SMEM = (size_t)SD * MT_LD * 4 + (size_t)SD * SD * 4;
+constexpr int JB = 32;                 // rows of H_start(j+1) per join block
+constexpr int JOIN_BLOCKS = SD / JB;   // join blocks per v-head
+constexpr int P_LD = SD + 4;           // padded row of the p tile (fp32)
+constexpr size_t FIN_SMEM = (size_t)SD * SD * 4 + (size_t)64 * P_LD * 4;
 
-// One block per v-head: H_start(1) = the real state (segment 0's end), H_start(j+1) =
-// M_j H_start(j) + N_j; H_start(j) kept for the correction, the last one written back as the
-// stream's final state. Thread (tr, tc) computes rows 8tr.. and columns 8tc.. of each product.
-__global__ void __launch_bounds__(256) seg_join_kernel(int S, const uint64_t *ptrs, const float *Nb,
-                                                       const float *Mb, float *Hs) {
-    float *h_real = reinterpret_cast<float *>(ptrs[0]);  // the stream's own state
-    extern __shared__ float js[];
-    float *mt = js;               // M^T [k][c], row MT_LD
-    float *hc = js + SD * MT_LD;  // H_start(j) [k][d]
-    const int j_head = blockIdx.x;
-    const int64_t per = (int64_t)gridDim.x * SD * SD;
-    const int64_t hoff = (int64_t)j_head * SD * SD;
-    const int tid = threadIdx.x, tr = tid >> 4, tcol = tid & 15;
-    float *hreal = h_real + hoff;
-    for (int i = tid; i < SD * SD; i += 256) {
-        const float v = hreal[i];
-        hc[i] = v;
-        Hs[hoff + i] = v;  // H_start(1)
-    }
-    for (int j = 1; j < S; ++j) {
+// Step j of the join and the correction of segment j, both from H_start(j) = Hs[j-1]:
+//  - blocks [0, Hv * JOIN_BLOCKS): rows 32 r .. of H_start(j+1) = M_j H_start(j) + N_j, written
+//    to Hs[j], or to the stream's state for the last step; thread (row pair, 8 columns);
+//  - the rest: a 64-token tile of segment j for one v-head, out[t] += H_start(j)^T p_t
+//    (thread: 4 tokens x 8 channels).
+__global__ void __launch_bounds__(256) seg_finish_kernel(SegPlan plan, int j, int Hv,
+                                                         const float *Nb, const float *Mb,
+                                                         float *Hs, const uint64_t *h_state,
+                                                         const __nv_bfloat16 *pbuf,
+                                                         __nv_bfloat16 *out) {
+    extern __shared__ float fs[];
+    const int tid = threadIdx.x;
+    const int64_t per = (int64_t)Hv * SD * SD;
+    const int nj = Hv * JOIN_BLOCKS;  // every step has a join (the last writes the final state)
+    float *h = fs;  // H_start(j) [k][d]
+    if ((int)blockIdx.x < nj) {
+        const int head = blockIdx.x / JOIN_BLOCKS, rb = blockIdx.x % JOIN_BLOCKS;
+        const int64_t hoff = (int64_t)head * SD * SD;
+        const float *H = Hs + (j - 1) * per + hoff;
         const float *M = Mb + (j - 1) * per + hoff;
         const float *N = Nb + (j - 1) * per + hoff;
-        for (int i = tid; i < SD * SD; i += 256) mt[(i % SD) * MT_LD + i / SD] = M[i];
+        float *mrow = fs + SD * SD;  // rows 32 rb .. of M_j [32][P_LD]
+        for (int i = tid; i < SD * SD / 4; i += 256)
+            reinterpret_cast<float4 *>(h)[i] = reinterpret_cast<const float4 *>(H)[i];
+        for (int i = tid; i < JB * SD / 4; i += 256) {
+            const int r = i / (SD / 4), c4 = i % (SD / 4);
+            *reinterpret_cast<float4 *>(mrow + r * P_LD + 4 * c4) =
+                *reinterpret_cast<const float4 *>(M + (int64_t)(JB * rb + r) * SD + 4 * c4);
+        }
         __syncthreads();
-        float acc[8][8];
+        const int r2 = tid >> 4, c8 = tid & 15;  // rows 2 r2, 2 r2 + 1; columns 8 c8 ..
+        float acc[2][8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) acc[r][c] = N[(int64_t)(8 * tr + r) * SD + 8 * tcol + c];
+            for (int c = 0; c < 8; ++c)
+                acc[r][c] = N[(int64_t)(JB * rb + 2 * r2 + r) * SD + 8 * c8 + c];
         for (int k = 0; k < SD; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(mt + k * MT_LD + 8 * tr);
-            const float4 a1 = *reinterpret_cast<const float4 *>(mt + k * MT_LD + 8 * tr + 4);
-            const float4 b0 = *reinterpret_cast<const float4 *>(hc + k * SD + 8 * tcol);
-            const float4 b1 = *reinterpret_cast<const float4 *>(hc + k * SD + 8 * tcol + 4);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float m0 = mrow[(2 * r2) * P_LD + k], m1 = mrow[(2 * r2 + 1) * P_LD + k];
+            const float4 b0 = *reinterpret_cast<const float4 *>(h + k * SD + 8 * c8);
+            const float4 b1 = *reinterpret_cast<const float4 *>(h + k * SD + 8 * c8 + 4);
             const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
-        }
-        __syncthreads();  // every thread is done reading hc and mt
-        float *dst = (j + 1 < S) ? Hs + j * per + hoff : hreal;
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const int idx = (8 * tr + r) * SD + 8 * tcol + c;
-                hc[idx] = acc[r][c];
-                dst[idx] = acc[r][c];
+                acc[0][c] = fmaf(m0, bv[c], acc[0][c]);
+                acc[1][c] = fmaf(m1, bv[c], acc[1][c]);
             }
-        __syncthreads();
+        }
+        float *dst = (j + 1 < plan.S) ? Hs + j * per + hoff
+                                      : reinterpret_cast<float *>(h_state[0]) + hoff;
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; c += 4)
+                *reinterpret_cast<float4 *>(dst + (int64_t)(JB * rb + 2 * r2 + r) * SD + 8 * c8 + c) =
+                    make_float4(acc[r][c], acc[r][c + 1], acc[r][c + 2], acc[r][c + 3]);
+        return;
     }
-}
-
-constexpr int PT_LD = 68;  // padded row of the transposed p tile
-constexpr size_t CORR_SMEM = (size_t)SD * SD * 4 + (size_t)SD * PT_LD * 4;
-
-// out[t][j] += H_start(seg)^T p_t for the 64-token tile blockIdx.x of the tokens past segment 0
-// (tiles never straddle a boundary: boundaries are multiples of 64), v-head blockIdx.y. Thread
-// (tg, dg) computes tokens 4tg.. and channels 8dg.. of the tile.
-__global__ void __launch_bounds__(256) seg_correct_kernel(SegPlan plan, int Hv, int total,
-                                                          const float *Hs,
-                                                          const __nv_bfloat16 *pbuf,
-                                                          __nv_bfloat16 *out) {
-    extern __shared__ float cs[];
-    float *h = cs;             // H_start [c][d]
-    float *pt = cs + SD * SD;  // p^T [c][t], row PT_LD
-    const int j = blockIdx.y;
-    const int t_tile = plan.b[1] + 64 * blockIdx.x;
-    if (t_tile >= total) return;
-    int seg = 1;
-    while (seg + 1 < plan.S && t_tile >= plan.b[seg + 1]) ++seg;
-    const int64_t per = (int64_t)Hv * SD * SD;
-    const float *H = Hs + (seg - 1) * per + (int64_t)j * SD * SD;
-    const int tid = threadIdx.x;
+    // correction of segment j
+    const int cb = blockIdx.x - nj;
+    const int seg_len = plan.b[j + 1] - plan.b[j];
+    const int ntile = (seg_len + 63) / 64;
+    const int head = cb / ntile, tile = cb % ntile;
+    const int t_tile = plan.b[j] + 64 * tile;
+    const float *H = Hs + (j - 1) * per + (int64_t)head * SD * SD;
+    float *pt = fs + SD * SD;  // p tile [64][P_LD]
     for (int i = tid; i < SD * SD / 4; i += 256)
         reinterpret_cast<float4 *>(h)[i] = reinterpret_cast<const float4 *>(H)[i];
-    for (int i = tid; i < 64 * SD; i += 256) {
-        const int t = i / SD, c = i % SD;
-        pt[c * PT_LD + t] = t_tile + t < total
-            ? __bfloat162float(pbuf[((int64_t)(t_tile + t) * Hv + j) * SD + c]) : 0.f;
+    for (int i = tid; i < 64 * SD / 8; i += 256) {
+        const int t = i / (SD / 8), c8 = (i % (SD / 8)) * 8;
+        float v[8];
+        if (t_tile + t < plan.b[j + 1]) {
+            Vec16<__nv_bfloat16>::load(pbuf + ((int64_t)(t_tile + t) * Hv + head) * SD + c8, v);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        }
+        *reinterpret_cast<float4 *>(pt + t * P_LD + c8) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4 *>(pt + t * P_LD + c8 + 4) = make_float4(v[4], v[5], v[6], v[7]);
     }
     __syncthreads();
     const int tg = tid >> 4, dg = tid & 15;
@@ -148,22 +153,29 @@ __global__ void __launch_bounds__(256) seg_correct_kernel(SegPlan plan, int Hv, 
     for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
-    for (int c = 0; c < SD; ++c) {
-        const float4 pv = *reinterpret_cast<const float4 *>(pt + c * PT_LD + 4 * tg);
-        const float4 h0 = *reinterpret_cast<const float4 *>(h + c * SD + 8 * dg);
-        const float4 h1 = *reinterpret_cast<const float4 *>(h + c * SD + 8 * dg + 4);
-        const float p4[4] = {pv.x, pv.y, pv.z, pv.w};
-        const float h8[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    for (int c4 = 0; c4 < SD; c4 += 4) {
+        float pv[4][4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 4; ++r) {
+            const float4 q = *reinterpret_cast<const float4 *>(pt + (4 * tg + r) * P_LD + c4);
+            pv[r][0] = q.x; pv[r][1] = q.y; pv[r][2] = q.z; pv[r][3] = q.w;
+        }
 #pragma unroll
-            for (int d = 0; d < 8; ++d) acc[r][d] = fmaf(h8[d], p4[r], acc[r][d]);
+        for (int cc = 0; cc < 4; ++cc) {
+            const float4 h0 = *reinterpret_cast<const float4 *>(h + (c4 + cc) * SD + 8 * dg);
+            const float4 h1 = *reinterpret_cast<const float4 *>(h + (c4 + cc) * SD + 8 * dg + 4);
+            const float h8[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int d = 0; d < 8; ++d) acc[r][d] = fmaf(h8[d], pv[r][cc], acc[r][d]);
+        }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int t = t_tile + 4 * tg + r;
-        if (t >= total) continue;
-        __nv_bfloat16 *o = out + ((int64_t)t * Hv + j) * SD + 8 * dg;
+        if (t >= plan.b[j + 1]) continue;
+        __nv_bfloat16 *o = out + ((int64_t)t * Hv + head) * SD + 8 * dg;
         float ov[8];
         Vec16<__nv_bfloat16>::load(o, ov);
 #pragma unroll
@@ -233,7 +245,8 @@ cudaError_t launch_segmented(const RecArgs &a0, int segments, cudaStream_t st) {
     float *Hs = reinterpret_cast<float *>(ws + l.Hs);
     __nv_bfloat16 *pbuf = reinterpret_cast<__nv_bfloat16 *>(ws + l.P);
 
-    seg_setup_kernel<<<256, 256, 0, st>>>(plan, Hv, a0.h_ptrs, cu_p, cu_alt, ptrs, Nb, Mb, zero_v);
+    seg_setup_kernel<<<256, 256, 0, st>>>(plan, Hv, a0.h_ptrs, cu_p, cu_alt, ptrs, Nb, Mb, Hs,
+                                          zero_v);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     RecArgs a = a0;
@@ -251,18 +264,16 @@ cudaError_t launch_segmented(const RecArgs &a0, int segments, cudaStream_t st) {
     a.workspace_bytes = chunk_tc_workspace_bytes(a.B, 0);
     e = launch_chunk_tc(a, st);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(seg_join_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)JOIN_SMEM);
+    e = cudaFuncSetAttribute(seg_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)FIN_SMEM);
     if (e != cudaSuccess) return e;
-    // the real state pointer lives in device memory: the join reads it from the table the
-    // setup kernel filled (ptrs[0])
-    seg_join_kernel<<<Hv, 256, JOIN_SMEM, st>>>(S, ptrs, Nb, Mb, Hs);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(seg_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CORR_SMEM);
-    if (e != cudaSuccess) return e;
-    dim3 grid((total - plan.b[1] + 63) / 64, Hv);
-    seg_correct_kernel<<<grid, 256, CORR_SMEM, st>>>(plan, Hv, total, Hs, pbuf,
-                                                     reinterpret_cast<__nv_bfloat16 *>(a0.out));
+    for (int j = 1; j < S; ++j) {
+        const int ntile = (plan.b[j + 1] - plan.b[j] + 63) / 64;
+        seg_finish_kernel<<<Hv * JOIN_BLOCKS + Hv * ntile, 256, FIN_SMEM, st>>>(
+            plan, j, Hv, Nb, Mb, Hs, a0.h_ptrs, pbuf, reinterpret_cast<__nv_bfloat16 *>(a0.out));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 
