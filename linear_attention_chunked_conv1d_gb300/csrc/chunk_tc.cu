@@ -228,25 +228,6 @@ __device__ __forceinline__ void load_raw(const RecArgs &a, unsigned char *sm,
     }
 }
 
-// Packed pairs of fp32 (Blackwell f32x2 ALU ops; each lane rounds like the scalar op).
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 // bf16 pair (low half = first element) widened to an fp32 pair
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
     return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

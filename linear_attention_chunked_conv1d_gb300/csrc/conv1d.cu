@@ -128,6 +128,17 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
         }
     }
 
+    // warps whose channels all lie past the normalised heads (v) skip the L2 work entirely
+    const bool l2_warp = HD > 0 && __any_sync(0xffffffffu, do_l2);
+    // taps as packed pairs of channels (e0, e1), (e2, e3): the scalar fmaf chain's bits
+    uint64_t wp[K][N / 2], bp[N / 2];
+#pragma unroll
+    for (int h = 0; h < N / 2; ++h) {
+        bp[h] = pk2(br[2 * h], br[2 * h + 1]);
+#pragma unroll
+        for (int m = 0; m < K; ++m) wp[m][h] = pk2(wr[2 * h][m], wr[2 * h + 1][m]);
+    }
+
     // rows in groups of 4: the 4 loads are issued before any of them is used
     constexpr int G = 4;
     for (int g0 = r0; g0 < r1; g0 += G) {
@@ -145,14 +156,17 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
         for (int q = 0; q < G; ++q) {
             float y[N];
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-                float acc = br[e];
+            for (int h = 0; h < N / 2; ++h) {
+                uint64_t acc = bp[h];
 #pragma unroll
-                for (int m = 0; m < K - 1; ++m) acc = fmaf(wr[e][m], win[m][e], acc);
-                acc = fmaf(wr[e][K - 1], cur[q][e], acc);
-                y[e] = silu(acc);
+                for (int m = 0; m < K - 1; ++m)
+                    acc = fma2(wp[m][h], pk2(win[m][2 * h], win[m][2 * h + 1]), acc);
+                acc = fma2(wp[K - 1][h], pk2(cur[q][2 * h], cur[q][2 * h + 1]), acc);
+                upk2(acc, y[2 * h], y[2 * h + 1]);
             }
-            if constexpr (HD > 0) {
+#pragma unroll
+            for (int e = 0; e < N; ++e) y[e] = silu(y[e]);
+            if (HD > 0 && l2_warp) {
                 // round to the stored type, then the same reduction as the l2 launch
                 float ss = 0.f;
 #pragma unroll
