@@ -37,7 +37,9 @@
 // the units sharing that k-head to read the old state (a per-(stream, k-head) count).
 //
 // Precision: operands that are raw bf16 inputs use kind::f16; operands derived from fp32
-// values (state, T, U', decayed keys) use kind::tf32 with round-to-nearest conversion,
+// values (state, T, U', decayed keys) use kind::tf32 with round-to-nearest conversion, except
+// the two intermediate products of the block substitution (U'0 and Z, inside U' = R T^T),
+// which the next MMA reads from TMEM without that rounding step;
 // accumulation is fp32. Rows at or past a stream's end are removed by selects.
 #include <mutex>
 
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_BARS);
     uint64_t *bar_b = bar_a + 1;
     uint64_t *bar_c = reinterpret_cast<uint64_t *>(sm + SM_BARS + 40);  // state update done
+    uint64_t *bar_d = reinterpret_cast<uint64_t *>(sm + SM_BARS + 48);  // block-substitution steps
     volatile int *err = reinterpret_cast<volatile int *>(sm + SM_BARS + 16);
     volatile int *unit_sh = err + 1;
     volatile int *slow_sh = err + 2;
@@ -376,6 +379,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         tc::mbar_init(bar_a, 1);
         tc::mbar_init(bar_b, 1);
         tc::mbar_init(bar_c, 1);
+        tc::mbar_init(bar_d, 1);
         tc::fence_mbar_init();
     }
     // identity tile (bf16, K-major 64x64) for the transposing MMAs
@@ -901,7 +905,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
             }
 
-            // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM; S <- S diag(e^{gc_L})
+            // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
             if (!last) {  // V tile consumed by the identity MMA: next chunk's V (FRONT: the
@@ -911,13 +915,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 cp_async_commit();
             }
             {
-                const int t0c = C16 * part, c0 = D32 * part;
-                float v[16], vt[16], sv[D32];
+                const int t0c = C16 * part;
+                float v[16], vt[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + t0c), v);
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RUD + t0c), vt);
-#pragma unroll
-                for (int g = 0; g < D32 / 16; ++g)
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
@@ -925,85 +926,74 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     const float kh_t = KDA ? v[ii] : sf[SF_EG + t] * v[ii];
                     v[ii] = t < n ? tc::to_tf32(sf[SF_BETA + t] * (vt[ii] - kh_t)) : 0.f;
                 }
-                const float egL = KDA ? 0.f : sf[SF_EG + TC_C - 1];
-#pragma unroll
-                for (int ii = 0; ii < D32; ++ii) sv[ii] *= KDA ? sf[SF_EL + c0 + ii] : egL;
                 tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
                 if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);  // Z = R1
-#pragma unroll
-                for (int g = 0; g < D32 / 16; ++g)
-                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
                 tc::tmem_wait_st();
             }
             tc::fence_before_sync();
             __syncthreads();
 
-            // ---------------- U'0^T = R0^T T00^T
-            constexpr uint32_t id32 = tc::idesc(128, 32, tc::FMT_TF32);
+            // ---------------- block substitution, one thread: U'0^T = R0^T T00^T;
+            //   Z^T = R1^T - U'0^T A10^T (accumulated onto R1^T); U'1^T = Z^T T11^T (into the
+            //   P U' accumulator columns 0..31). Each product reads the previous one as its
+            //   A operand straight from TMEM, without the rounding step; MMAs into
+            //   different accumulators are not ordered, so the issuing thread waits on bar_d
+            //   (two completions per chunk: parities 0, then 1) between them.
             if (warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
+                constexpr uint32_t id32 = tc::idesc(128, 32, tc::FMT_TF32);
+                bool ok = true;
 #pragma unroll
                 for (uint32_t kk = 0; kk < 4; ++kk)
                     tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8,
                                     tc::sdesc_sw128((sb + SM_T00) + kk * 32u), id32, kk > 0);
-                tc::mma_commit(bar_b);
-            }
-            wait_bar(bar_b, phase_b);
-            if (!sync_ok(err)) break;
-            // U'0^T rounded to tf32 (A operand of the coupling MMA; also the final U'0^T)
-            {
-                const int c8 = 8 * part;
-                float v[8];
-                tc::tmem_ld8(tc::tmem_addr(tm, lq, COL_D6 + c8), v);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int ii = 0; ii < 8; ++ii) v[ii] = tc::to_tf32(v[ii]);
-                tc::tmem_st8(tc::tmem_addr(tm, lq, COL_RU + c8), v);
-                tc::tmem_wait_st();
-            }
-            tc::fence_before_sync();
-            __syncthreads();
-            // ---------------- Z^T = R1^T - U'0^T A10^T (accumulated onto R1^T)
-            if (warp == 0 && tc::elect_one()) {
+                tc::mma_commit(bar_d);
+                ok = tc::mbar_wait(bar_d, 0, WAIT_NS);
                 tc::fence_after_sync();
+                if (ok) {
 #pragma unroll
-                for (uint32_t kk = 0; kk < 4; ++kk)
-                    tc::mma_tf32_ts(tm + COL_D6 + 32, tm + COL_RU + kk * 8,
-                                    tc::sdesc_sw128((sb + SM_NA10) + kk * 32u), id32, 1);
+                    for (uint32_t kk = 0; kk < 4; ++kk)
+                        tc::mma_tf32_ts(tm + COL_D6 + 32, tm + COL_D6 + kk * 8,
+                                        tc::sdesc_sw128((sb + SM_NA10) + kk * 32u), id32, 1);
+                    tc::mma_commit(bar_d);
+                    ok = tc::mbar_wait(bar_d, 1, WAIT_NS);
+                    tc::fence_after_sync();
+                }
+                if (ok) {
+#pragma unroll
+                    for (uint32_t kk = 0; kk < 4; ++kk)
+                        tc::mma_tf32_ts(tm + COL_D4, tm + COL_D6 + 32 + kk * 8,
+                                        tc::sdesc_sw128((sb + SM_T11) + kk * 32u), id32, kk > 0);
+                } else {
+                    *err = 1;
+                }
                 tc::mma_commit(bar_b);
             }
-            wait_bar(bar_b, phase_b);
-            if (!sync_ok(err)) break;
-            // Z^T rounded to tf32 -> the R1 columns (A operand of the last MMA)
+            // S <- S diag(e^{gc_L}) while the tensor core works (the chain above reads none of
+            // the state columns; the state MMA is issued after the barriers below)
             {
-                const int c8 = 8 * part;
-                float v[8];
-                tc::tmem_ld8(tc::tmem_addr(tm, lq, COL_D6 + 32 + c8), v);
+                const int c0 = D32 * part;
+                float sv[D32];
+#pragma unroll
+                for (int g = 0; g < D32 / 16; ++g)
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
                 tc::tmem_wait_ld();
+                const float egL = KDA ? 0.f : sf[SF_EG + TC_C - 1];
 #pragma unroll
-                for (int ii = 0; ii < 8; ++ii) v[ii] = tc::to_tf32(v[ii]);
-                tc::tmem_st8(tc::tmem_addr(tm, lq, COL_RU + 32 + c8), v);
+                for (int ii = 0; ii < D32; ++ii) sv[ii] *= KDA ? sf[SF_EL + c0 + ii] : egL;
+#pragma unroll
+                for (int g = 0; g < D32 / 16; ++g)
+                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
                 tc::tmem_wait_st();
-            }
-            tc::fence_before_sync();
-            __syncthreads();
-            // ---------------- U'1^T = Z^T T11^T  (into the P U' accumulator columns 0..31)
-            if (warp == 0 && tc::elect_one()) {
-                tc::fence_after_sync();
-#pragma unroll
-                for (uint32_t kk = 0; kk < 4; ++kk)
-                    tc::mma_tf32_ts(tm + COL_D4, tm + COL_RU + 32 + kk * 8,
-                                    tc::sdesc_sw128((sb + SM_T11) + kk * 32u), id32, kk > 0);
-                tc::mma_commit(bar_b);
             }
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
 
             // ------ U'^T -> TMEM (tf32); GDN also U'^T diag(e^{gc_L - gc}) for the state update
             {
-                const int t0c = C16 * part;  // 16 columns: U'0 (rounded, in RU) or U'1 (D4)
+                const int t0c = C16 * part;  // 16 columns: U'0 (in D6) or U'1 (in D4)
                 float v[16], w[16];
-                if (t0c < 32) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                if (t0c < 32) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);
                 else tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c - 32), v);
                 tc::tmem_wait_ld();
 #pragma unroll
@@ -1011,7 +1001,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     v[ii] = tc::to_tf32(v[ii]);
                     w[ii] = KDA ? 0.f : tc::to_tf32(v[ii] * sf[SF_EGL + t0c + ii]);
                 }
-                if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
+                tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
                 if (!KDA) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RUD + t0c), w);
             }
             tc::tmem_wait_st();
