@@ -113,6 +113,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
+// Wait until at most the most recent committed group of this thread is still in flight.
+__device__ __forceinline__ void cp_async_wait_but_last() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -279,10 +283,8 @@ __device__ __forceinline__ void conv_tile(const RecArgs &a, unsigned char *sm, i
                 }
             }
             float y[4];
-            upk2(a01, y[0], y[1]);
-            upk2(a23, y[2], y[3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) y[e] = silu(y[e]);
+            upk2(silu2(a01), y[0], y[1]);
+            upk2(silu2(a23), y[2], y[3]);
             __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
             __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
             if (sec < 2) {
@@ -540,6 +542,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
         };
         int pend_tok0 = 0, pend_n = 0;  // output tile staged, not yet stored
+        bool staged_ahead = false;      // GDN: the chunk's tf32 K|Q tile is already staged
 
         for (int ch = 0; ch < nch; ++ch) {
             const int tok0 = t0 + ch * TC_C;
@@ -697,6 +700,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
                 tc::fence_async_smem();
             };
+            // the same copy of the next chunk's tile by warps 1-15, while warp 0 runs the
+            // block-substitution chain of this chunk (GDN, separate front end)
+            auto stage_state_operands_ahead = [&]() {
+#pragma unroll
+                for (int m = 0; m < 5; ++m) {
+                    const int idx = (tid - 32) + (TC_THREADS - 32) * m;
+                    if (idx >= 2048) break;
+                    const int r = idx >> 4, cj = idx & 15;
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        f[2 * e] = __uint_as_float(w4[e] << 16);
+                        f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
+                    }
+                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8, 128, 4)) =
+                        make_float4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8 + 4, 128, 4)) =
+                        make_float4(f[4], f[5], f[6], f[7]);
+                }
+                tc::fence_async_smem();
+            };
             // D2 = S [K;Q]^T (tf32, A from TMEM) and V^T (identity MMA) into the U'd columns
             auto issue_mma2 = [&]() {
                 tc::fence_before_sync();
@@ -721,7 +747,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             };
 
             if (!KDA) {  // GDN: stage while D1 and K^T are computed, then start the state MMA
-                stage_state_operands();
+                if (!staged_ahead) stage_state_operands();
+                staged_ahead = false;
                 wait_state();
                 issue_mma2();
             }
@@ -930,6 +957,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);  // Z = R1
                 tc::tmem_wait_st();
             }
+            // GDN, separate front end: the next chunk's K|Q copies (issued once D1 was read;
+            // the V copies just issued may stay in flight) have landed for every thread after
+            // the barrier below, and its tf32 copy can be staged during the chain
+            const bool stage_ahead = !KDA && !FRONT && !last;
+            if (stage_ahead) cp_async_wait_but_last();
             tc::fence_before_sync();
             __syncthreads();
 
@@ -985,6 +1017,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 for (int g = 0; g < D32 / 16; ++g)
                     tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
                 tc::tmem_wait_st();
+            }
+            if (stage_ahead) {  // the D2 MMA of this chunk, the tile's one reader, is complete
+                if (warp != 0) stage_state_operands_ahead();
+                staged_ahead = true;
             }
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;

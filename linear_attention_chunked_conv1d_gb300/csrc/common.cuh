@@ -80,11 +80,6 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
     return __float2bfloat16_rn(x);
 }
 
-// SiLU(y) = y sigmoid(y) = y / (1 + e^-y), with the fast exponential and reciprocal. The conv
-// kernel and the fused front end of the tensor-core recurrence both use it, so that the two
-// paths give identical bits.
-__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.f + __expf(-y)); }
-
 // Packed pairs of fp32 (Blackwell f32x2 ALU ops; each lane rounds like the scalar op, so a
 // packed chain gives the bits of the scalar one).
 __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
@@ -104,6 +99,40 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Hardware base-2 exponential and reciprocal (approximate, subnormals flushed).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// SiLU(y) = y sigmoid(y) = y / (1 + e^-y), with e^-y = 2^(-y log2 e) and the reciprocal from
+// the hardware approximations. silu2 applies it to a packed pair with the same roundings, so
+// every caller (the conv kernel, the fused front end and the gated epilogues) gets the bits of
+// the scalar form.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float silu(float y) {
+    const float e = ex2_approx(__fmul_rn(y, -kLog2e));
+    return __fmul_rn(y, rcp_approx(__fadd_rn(1.f, e)));
+}
+__device__ __forceinline__ uint64_t silu2(uint64_t y) {
+    float t0, t1;
+    upk2(mul2(y, pk2(-kLog2e, -kLog2e)), t0, t1);
+    float d0, d1;
+    upk2(add2(pk2(1.f, 1.f), pk2(ex2_approx(t0), ex2_approx(t1))), d0, d1);
+    return mul2(y, pk2(rcp_approx(d0), rcp_approx(d1)));
 }
 
 // Raises a device status flag (LA_DEV_*). `status` points at the library's per-device word.

@@ -139,14 +139,16 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
         for (int m = 0; m < K; ++m) wp[m][h] = pk2(wr[2 * h][m], wr[2 * h + 1][m]);
     }
 
+    const T *xp = x + (int64_t)r0 * xs + c0;
+    T *op = out + (int64_t)r0 * os + c0;
     // rows in groups of 4: the 4 loads are issued before any of them is used
     constexpr int G = 4;
-    for (int g0 = r0; g0 < r1; g0 += G) {
+    for (int g0 = r0; g0 < r1; g0 += G, xp += G * xs, op += G * os) {
         float cur[G][N];
 #pragma unroll
         for (int q = 0; q < G; ++q) {
             if (active && g0 + q < r1) {
-                V::load(x + (int64_t)(g0 + q) * xs + c0, cur[q]);
+                V::load(xp + q * xs, cur[q]);
             } else {
 #pragma unroll
                 for (int e = 0; e < N; ++e) cur[q][e] = 0.f;
@@ -162,10 +164,8 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                 for (int m = 0; m < K - 1; ++m)
                     acc = fma2(wp[m][h], pk2(win[m][2 * h], win[m][2 * h + 1]), acc);
                 acc = fma2(wp[K - 1][h], pk2(cur[q][2 * h], cur[q][2 * h + 1]), acc);
-                upk2(acc, y[2 * h], y[2 * h + 1]);
+                upk2(silu2(acc), y[2 * h], y[2 * h + 1]);
             }
-#pragma unroll
-            for (int e = 0; e < N; ++e) y[e] = silu(y[e]);
             if (HD > 0 && l2_warp) {
                 // round to the stored type, then the same reduction as the l2 launch
                 float ss = 0.f;
@@ -183,7 +183,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                     for (int e = 0; e < N; ++e) y[e] *= inv;
                 }
             }
-            if (active && g0 + q < r1) V::store(out + (int64_t)(g0 + q) * os + c0, y);
+            if (active && g0 + q < r1) V::store(op + q * os, y);
             if constexpr (K > 1) {
 #pragma unroll
                 for (int m = 0; m < K - 2; ++m)
