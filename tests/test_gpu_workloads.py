@@ -80,3 +80,41 @@ def test_kda_t4096_pad_fill_identical(cuda):
             outs.append((p.out.clone(), inp["h"].clone(), inp["conv_state"].clone()))
         for a, b in zip(*outs):
             assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["gdn_batched_8x2048_h16_d128", "kda_t4096_h32_d128"])
+@pytest.mark.parametrize("mode", ["split", "fused"])
+def test_graph_replay_equals_direct_calls(cuda, name, mode):
+    """The bench also times each path as a CUDA-graph replay of the same public calls: two
+    replayed steps must give the bits of two directly launched ones (outputs, h states, conv
+    states), from the same inputs."""
+    wl = WORKLOADS[name]
+    res = []
+    for graphed in (False, True):  # the direct run first: it also loads every kernel
+        inp = make_inputs(wl, device=cuda, seed=3)
+        p = PrefillPass(wl, inp)
+
+        def body():
+            if mode == "fused":
+                p.fused()
+            else:
+                p.front_end()
+                p.recurrence()
+        if graphed:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                body()  # recorded, not run: the inputs are still the initial ones
+            torch.cuda.synchronize()
+            g.replay()
+            g.replay()
+        else:
+            body()
+            body()
+        torch.cuda.synchronize()
+        res.append((p.out.clone(), inp["h"].clone(), inp["conv_state"].clone()))
+        del p, inp
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+    torch.cuda.empty_cache()
