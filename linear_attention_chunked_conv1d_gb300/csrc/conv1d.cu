@@ -141,8 +141,9 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 
     const T *xp = x + (int64_t)r0 * xs + c0;
     T *op = out + (int64_t)r0 * os + c0;
-    // rows in groups of 4: the 4 loads are issued before any of them is used
-    constexpr int G = 4;
+    // rows in groups of 6: the 6 loads are issued before any of them is used (6 keeps the
+    // kernel at 8 blocks of 128 threads per SM; 8 would need more registers than that allows)
+    constexpr int G = 6;
     for (int g0 = r0; g0 < r1; g0 += G, xp += G * xs, op += G * os) {
         float cur[G][N];
 #pragma unroll
