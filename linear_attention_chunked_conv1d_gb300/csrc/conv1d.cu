@@ -27,6 +27,60 @@ __device__ __forceinline__ int conv_run_base(const int32_t *cu, int s) {
     return cu[s] / CONV_ROWS + s;
 }
 
+// One output row of a thread's 4 channels: y = SiLU(b + sum_m w_m xh_m) over the K-1 window
+// rows and the current row, then (HD > 0, in a warp that holds normalised channels) rounded to
+// T and scaled by 1/sqrt(sum of squares of the head + eps). Every lane of the warp calls it.
+template <typename T, int K, int HD>
+__device__ __forceinline__ void conv_row(const uint64_t (&wp)[K][2], const uint64_t (&bp)[2],
+                                         const float (&win)[K > 1 ? K - 1 : 1][4],
+                                         const float (&cur)[4], bool l2_warp, bool do_l2,
+                                         float eps, float (&y)[4]) {
+    constexpr int LPH = HD > 0 ? HD / 4 : 1;  // lanes per head
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint64_t acc = bp[h];
+#pragma unroll
+        for (int m = 0; m < K - 1; ++m)
+            acc = fma2(wp[m][h], pk2(win[m][2 * h], win[m][2 * h + 1]), acc);
+        acc = fma2(wp[K - 1][h], pk2(cur[2 * h], cur[2 * h + 1]), acc);
+        upk2(silu2(acc), y[2 * h], y[2 * h + 1]);
+    }
+    if (HD > 0 && l2_warp) {
+        // round to the stored type, then the same reduction as the l2 launch
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            y[e] = to_f(from_f<T>(y[e]));
+            ss = fmaf(y[e], y[e], ss);
+        }
+#pragma unroll
+        for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (do_l2) {
+            const float inv = rsqrtf(ss + eps);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[e] *= inv;
+        }
+    }
+}
+
+// Taps and bias of a thread's 4 channels as packed pairs (e0, e1), (e2, e3).
+template <typename T, int K>
+__device__ __forceinline__ void load_taps(const T *w, const T *bias, int c0, bool active,
+                                          uint64_t (&wp)[K][2], uint64_t (&bp)[2]) {
+    float wr[4][K], br[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int j = 0; j < K; ++j) wr[e][j] = active ? to_f(w[(int64_t)(c0 + e) * K + j]) : 0.f;
+    if (bias && active) Vec4<T>::load(bias + c0, br);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        bp[h] = pk2(br[2 * h], br[2 * h + 1]);
+#pragma unroll
+        for (int m = 0; m < K; ++m) wp[m][h] = pk2(wr[2 * h][m], wr[2 * h + 1][m]);
+    }
+}
+
 // HD > 0: also L2-normalise, per (token, head), the first n_l2 channels (whole heads of HD
 // channels). The conv output is rounded to T first, exactly as the separate l2 launch would
 // read it back, and the sum of squares is reduced in the same order as that launch, so the
@@ -37,10 +91,9 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                    const T *__restrict__ x, const T *__restrict__ w,
                    const T *__restrict__ bias, T *__restrict__ out,
                    const int32_t *__restrict__ cu, int B, int total, int C, int64_t xs,
-                   int64_t os, int n_l2, float eps, int *status, bool one_per_stream) {
+                   int64_t os, int n_l2, float eps, int *status) {
     using V = Vec4<T>;
     constexpr int N = V::N;
-    constexpr int LPH = HD > 0 ? HD / N : 1;  // lanes per head
     const int cv = blockIdx.y * CONV_THREADS + threadIdx.x;
     const int c0 = cv * N;
     const bool active = c0 < C;  // inactive lanes still take part in the head reductions
@@ -48,12 +101,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 
     // Which stream and which run of it this block covers.
     int s = 0, sb = 0, se = total, run = blockIdx.x;
-    if (one_per_stream) {  // decode: row s is the one token of stream s
-        s = blockIdx.x;
-        sb = s;
-        se = s + 1;
-        run = 0;
-    } else if (cu) {
+    if (cu) {
         if (cu[0] != 0 || cu[B] != total) {
             if (threadIdx.x == 0) raise_status(status, LA_DEV_BAD_SEQLENS);
             return;
@@ -77,15 +125,8 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
     if (run < 0 || r0 >= se) return;  // slot past this stream's runs (uniform per block)
     const int r1 = min(r0 + CONV_ROWS, se);
 
-    float wr[N][K];
-    float br[N];
-#pragma unroll
-    for (int e = 0; e < N; ++e) {
-        br[e] = 0.f;
-#pragma unroll
-        for (int j = 0; j < K; ++j) wr[e][j] = active ? to_f(w[(int64_t)(c0 + e) * K + j]) : 0.f;
-    }
-    if (bias && active) V::load(bias + c0, br);
+    uint64_t wp[K][2], bp[2];
+    load_taps<T, K>(w, bias, c0, active, wp, bp);
 
     // win[m] = row (tau - (K-1) + m) of xh = [state ; x] for the current tau.
     float win[K > 1 ? K - 1 : 1][N];
@@ -130,14 +171,6 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 
     // warps whose channels all lie past the normalised heads (v) skip the L2 work entirely
     const bool l2_warp = HD > 0 && __any_sync(0xffffffffu, do_l2);
-    // taps as packed pairs of channels (e0, e1), (e2, e3): the scalar fmaf chain's bits
-    uint64_t wp[K][N / 2], bp[N / 2];
-#pragma unroll
-    for (int h = 0; h < N / 2; ++h) {
-        bp[h] = pk2(br[2 * h], br[2 * h + 1]);
-#pragma unroll
-        for (int m = 0; m < K; ++m) wp[m][h] = pk2(wr[2 * h][m], wr[2 * h + 1][m]);
-    }
 
     const T *xp = x + (int64_t)r0 * xs + c0;
     T *op = out + (int64_t)r0 * os + c0;
@@ -158,32 +191,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 #pragma unroll
         for (int q = 0; q < G; ++q) {
             float y[N];
-#pragma unroll
-            for (int h = 0; h < N / 2; ++h) {
-                uint64_t acc = bp[h];
-#pragma unroll
-                for (int m = 0; m < K - 1; ++m)
-                    acc = fma2(wp[m][h], pk2(win[m][2 * h], win[m][2 * h + 1]), acc);
-                acc = fma2(wp[K - 1][h], pk2(cur[q][2 * h], cur[q][2 * h + 1]), acc);
-                upk2(silu2(acc), y[2 * h], y[2 * h + 1]);
-            }
-            if (HD > 0 && l2_warp) {
-                // round to the stored type, then the same reduction as the l2 launch
-                float ss = 0.f;
-#pragma unroll
-                for (int e = 0; e < N; ++e) {
-                    y[e] = to_f(from_f<T>(y[e]));
-                    ss = fmaf(y[e], y[e], ss);
-                }
-#pragma unroll
-                for (int off = LPH / 2; off > 0; off >>= 1)
-                    ss += __shfl_xor_sync(0xffffffffu, ss, off);
-                if (do_l2) {
-                    const float inv = rsqrtf(ss + eps);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) y[e] *= inv;
-                }
-            }
+            conv_row<T, K, HD>(wp, bp, win, cur[q], l2_warp, do_l2, eps, y);
             if (active && g0 + q < r1) V::store(op + q * os, y);
             if constexpr (K > 1) {
 #pragma unroll
@@ -197,19 +205,69 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
     }
 }
 
+// One new token per stream (decode): row s of x is the token of stream s. A block takes
+// STEP_STREAMS streams for its 128 x 4 channels, so the taps are read once per 8 streams; each
+// stream's state is read, the row computed by the same conv_row as above, and the state
+// advanced by that one row.
+constexpr int STEP_STREAMS = 8;
+
+template <typename T, int K, int HD>
+__global__ void __launch_bounds__(CONV_THREADS)
+conv1d_silu_step_kernel(const uint64_t *__restrict__ state_ptrs, const T *__restrict__ x,
+                        const T *__restrict__ w, const T *__restrict__ bias, T *__restrict__ out,
+                        int B, int C, int64_t xs, int64_t os, int n_l2, float eps) {
+    using V = Vec4<T>;
+    const int c0 = (blockIdx.y * CONV_THREADS + threadIdx.x) * 4;
+    const bool active = c0 < C;
+    const bool do_l2 = HD > 0 && c0 < n_l2;
+    const bool l2_warp = HD > 0 && __any_sync(0xffffffffu, do_l2);
+    uint64_t wp[K][2], bp[2];
+    load_taps<T, K>(w, bias, c0, active, wp, bp);
+    const int s_end = min(B, (int)(blockIdx.x + 1) * STEP_STREAMS);
+    for (int s = blockIdx.x * STEP_STREAMS; s < s_end; ++s) {  // uniform over the block
+        float win[K > 1 ? K - 1 : 1][4] = {};
+        float cur[4] = {0.f, 0.f, 0.f, 0.f};
+        T *st = K > 1 ? reinterpret_cast<T *>(state_ptrs[s]) : nullptr;
+        if (active) {
+            if constexpr (K > 1) {
+#pragma unroll
+                for (int m = 0; m < K - 1; ++m) V::load(st + (int64_t)m * C + c0, win[m]);
+            }
+            V::load(x + (int64_t)s * xs + c0, cur);
+        }
+        float y[4];
+        conv_row<T, K, HD>(wp, bp, win, cur, l2_warp, do_l2, eps, y);
+        if (active) {
+            V::store(out + (int64_t)s * os + c0, y);
+            if constexpr (K > 1) {
+#pragma unroll
+                for (int m = 0; m < K - 2; ++m) V::store(st + (int64_t)m * C + c0, win[m + 1]);
+                V::store(st + (int64_t)(K - 2) * C + c0, cur);
+            }
+        }
+    }
+}
+
 template <typename T, int K, int HD>
 static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
+    if (a.one_per_stream) {
+        const int nvec = a.channels / 4;
+        dim3 grid((a.B + STEP_STREAMS - 1) / STEP_STREAMS, (nvec + CONV_THREADS - 1) / CONV_THREADS);
+        conv1d_silu_step_kernel<T, K, HD><<<grid, CONV_THREADS, 0, st>>>(
+            a.state_ptrs, (const T *)a.x, (const T *)a.w, (const T *)a.bias, (T *)a.out, a.B,
+            a.channels, a.x_stride, a.out_stride, a.l2_heads * a.head_dim, a.eps);
+        return cudaGetLastError();
+    }
     constexpr int N = Vec4<T>::N;
     int nvec = a.channels / N;
     // Run slots: single stream ceil(total/ROWS); varlen floor(total/ROWS) + B covers every
     // stream's runs (stream s starts at slot floor(cu[s]/ROWS) + s).
-    int slots = a.one_per_stream ? a.B
-                : a.cu ? a.total / CONV_ROWS + a.B : (a.total + CONV_ROWS - 1) / CONV_ROWS;
+    int slots = a.cu ? a.total / CONV_ROWS + a.B : (a.total + CONV_ROWS - 1) / CONV_ROWS;
     dim3 grid(slots, (nvec + CONV_THREADS - 1) / CONV_THREADS);
     conv1d_silu_kernel<T, K, HD><<<grid, CONV_THREADS, 0, st>>>(
         a.state_ptrs, (T *)a.single_state, (const T *)a.x, (const T *)a.w, (const T *)a.bias,
         (T *)a.out, a.cu, a.B, a.total, a.channels, a.x_stride, a.out_stride,
-        a.l2_heads * a.head_dim, a.eps, a.status, a.one_per_stream);
+        a.l2_heads * a.head_dim, a.eps, a.status);
     return cudaGetLastError();
 }
 
