@@ -723,10 +723,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
                 tc::fence_async_smem();
             };
-            // D2 = S [K;Q]^T (tf32, A from TMEM) and V^T (identity MMA) into the U'd columns
+            // D2 = S [K;Q]^T (tf32, A from TMEM) and V^T (identity MMA) into the U'd columns.
+            // Issued by warp 0 while warps 8-15 solve the triangular blocks: the issuing lane
+            // is held for as long as the tensor core takes to run the group, and warp 0 has no
+            // share in that solve (the barrier before it made the staged operands visible).
             auto issue_mma2 = [&]() {
-                tc::fence_before_sync();
-                __syncthreads();
                 if (warp == 0 && tc::elect_one()) {
                     tc::fence_after_sync();
                     constexpr uint32_t id = tc::idesc(128, 128, tc::FMT_TF32);
@@ -746,11 +747,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
             };
 
-            if (!KDA) {  // GDN: stage while D1 and K^T are computed, then start the state MMA
+            if (!KDA) {  // GDN: stage while D1 and K^T are computed (unless staged ahead)
                 if (!staged_ahead) stage_state_operands();
                 staged_ahead = false;
+                // the previous state update must be complete before the K^T tile below is
+                // rewritten and before D2 reads S
                 wait_state();
-                issue_mma2();
             }
 
             if (pend_n > 0) {  // previous chunk's output while D1 is computed
@@ -861,6 +863,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
             }
             tc::fence_async_smem();
+            tc::fence_before_sync();
             __syncthreads();
 
             if (KDA) {  // KDA: the Kl|Ql and Kr buffers are free now
@@ -884,35 +887,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     }
                 }
                 tc::fence_async_smem();
-                issue_mma2();
+                tc::fence_before_sync();
+                __syncthreads();
             }
 
             // ---------------- T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} (the two 32-token
-            //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores, 8
-            //   threads per column (rows 8m + p). The coupling block is applied by the tensor
-            //   core as a block substitution: U'0 = R0 T00^T, U'1 = (R1 - U'0 A10^T) T11^T.
-            {
-                const int b = warp >> 3, o = 32 * b;
-                const int jj = 4 * (warp & 7) + (lane >> 3), p = lane & 7;
-                float x[4];
+            //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores by
+            //   warps 8-15, 4 lanes per column (rows 4m + p); meanwhile warp 0 issues D2. The
+            //   coupling block is applied by the tensor core as a block substitution:
+            //   U'0 = R0 T00^T, U'1 = (R1 - U'0 A10^T) T11^T.
+            if (warp >= 8) {
+                const int w8 = warp - 8, b = w8 >> 2, o = 32 * b;
+                const int jj = 8 * (w8 & 3) + (lane >> 2), p = lane & 3;
+                float x[8];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) x[m] = (8 * m + p == jj) ? 1.f : 0.f;
-                const float *ab = atp + o * AT_LD + o + p;  // ab[i*AT_LD + 8m] = A[o+8m+p][o+i]
+                for (int m = 0; m < 8; ++m) x[m] = (4 * m + p == jj) ? 1.f : 0.f;
+                const float *ab = atp + o * AT_LD + o + p;  // ab[i*AT_LD + 4m] = A[o+4m+p][o+i]
 #pragma unroll
                 for (int i = 0; i < 31; ++i) {
-                    const int m0 = i >> 3;
-                    const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~7) | (i & 7));
+                    const int m0 = i >> 2;
+                    const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~3) | (i & 3));
                     {
-                        const float nx = fmaf(-ab[i * AT_LD + 8 * m0], xi, x[m0]);
-                        x[m0] = (p > (i & 7)) ? nx : x[m0];
+                        const float nx = fmaf(-ab[i * AT_LD + 4 * m0], xi, x[m0]);
+                        x[m0] = (p > (i & 3)) ? nx : x[m0];
                     }
 #pragma unroll
-                    for (int m = m0 + 1; m < 4; ++m) x[m] = fmaf(-ab[i * AT_LD + 8 * m], xi, x[m]);
+                    for (int m = m0 + 1; m < 8; ++m) x[m] = fmaf(-ab[i * AT_LD + 4 * m], xi, x[m]);
                 }
                 const uint32_t tile = b == 0 ? SM_T00 : SM_T11;
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    st_tf32(sm, tile + tc::sw128_offset(8 * m + p, jj, 32, 4), x[m]);
+                for (int m = 0; m < 8; ++m)
+                    st_tf32(sm, tile + tc::sw128_offset(4 * m + p, jj, 32, 4), x[m]);
+            } else if (warp == 0) {
+                issue_mma2();
             }
             tc::fence_async_smem();
             __syncthreads();
