@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 cp_async_commit();
             }
 
-            // ---------------- A^T (fp32) and P (tf32) from D1; GDN: K^T tile
+            // ---------------- A^T (fp32) and P (tf32) from D1
             {
                 const int r = row & 63;
                 const bool isq = row >= 64;
@@ -812,9 +812,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 const bool split_ok = KDA || (-gm_ <= 80.f && gm_ - sf[SF_GC + TC_C - 1] <= 80.f);
                 const float gct2 = KDA ? 0.f : sf[SF_GC2 + r];
                 const float rowf = (KDA ? 1.f : sf[SF_RF + r]) * (isq ? 1.f : bt);
-                float v[16], kt[16];
+                float v[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D1 + i0), v);
-                if (!KDA) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + i0), kt);
                 tc::tmem_wait_ld();
                 if (KDA || split_ok) {
 #pragma unroll
@@ -848,17 +847,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                             *reinterpret_cast<float4 *>(sm + SM_NA10 + tc::sw128_offset(r - 32, i0 + q4 * 4, 32, 4)) =
                                 make_float4(tc::to_tf32(-v[q4 * 4]), tc::to_tf32(-v[q4 * 4 + 1]),
                                             tc::to_tf32(-v[q4 * 4 + 2]), tc::to_tf32(-v[q4 * 4 + 3]));
-                    }
-                }
-                if (!KDA) {
-                    // K^T[c][t] (exact in tf32) -> the [c][t] tile; columns t >= n zeroed
-                    const int c = row;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int t = i0 + q4 * 4;
-                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, t, 128, 4)) =
-                            make_float4(t + 0 < n ? kt[q4 * 4 + 0] : 0.f, t + 1 < n ? kt[q4 * 4 + 1] : 0.f,
-                                        t + 2 < n ? kt[q4 * 4 + 2] : 0.f, t + 3 < n ? kt[q4 * 4 + 3] : 0.f);
                     }
                 }
             }
@@ -918,8 +906,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
                     st_tf32(sm, tile + tc::sw128_offset(4 * m + p, jj, 32, 4), x[m]);
-            } else if (warp == 0) {
-                issue_mma2();
+            } else {
+                if (warp == 0) issue_mma2();
+                if (!KDA) {
+                    // K^T[c][t] (exact in tf32) -> the [c][t] tile, columns t >= n zeroed: warps
+                    // 0-7, two 16-column groups per thread (the solve leaves them idle)
+                    const int c = row;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i0 = 16 * (warp >> 2) + 32 * h;
+                        float kt[16];
+                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + i0), kt);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int t = i0 + q4 * 4;
+                            *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, t, 128, 4)) =
+                                make_float4(t + 0 < n ? kt[q4 * 4 + 0] : 0.f, t + 1 < n ? kt[q4 * 4 + 1] : 0.f,
+                                            t + 2 < n ? kt[q4 * 4 + 2] : 0.f, t + 3 < n ? kt[q4 * 4 + 3] : 0.f);
+                        }
+                    }
+                }
             }
             tc::fence_async_smem();
             __syncthreads();
