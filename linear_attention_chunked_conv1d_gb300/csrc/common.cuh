@@ -51,12 +51,27 @@ template <> struct Vec4<float> {
     static constexpr int N = 4;
     __device__ __forceinline__ static void load(const float *p, float *f) { Vec16<float>::load(p, f); }
     __device__ __forceinline__ static void store(float *p, const float *f) { Vec16<float>::store(p, f); }
+    // the access as loaded (kept in this form while in flight), and its widening
+    using Raw = float4;
+    __device__ __forceinline__ static Raw load_raw(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+    __device__ __forceinline__ static Raw zero_raw() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ static void widen(const Raw &v, float *f) {
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
 };
 
 template <> struct Vec4<__nv_bfloat16> {
     static constexpr int N = 4;
     __device__ __forceinline__ static void load(const __nv_bfloat16 *p, float *f) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        widen(load_raw(p), f);
+    }
+    // the access as loaded (two registers while in flight), and its exact widening
+    using Raw = uint2;
+    __device__ __forceinline__ static Raw load_raw(const __nv_bfloat16 *p) {
+        return *reinterpret_cast<const uint2 *>(p);
+    }
+    __device__ __forceinline__ static Raw zero_raw() { return make_uint2(0u, 0u); }
+    __device__ __forceinline__ static void widen(const Raw &v, float *f) {
         f[0] = __uint_as_float(v.x << 16);
         f[1] = __uint_as_float(v.x & 0xFFFF0000u);
         f[2] = __uint_as_float(v.y << 16);

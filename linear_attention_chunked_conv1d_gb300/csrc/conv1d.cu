@@ -21,6 +21,7 @@ namespace la {
 
 constexpr int CONV_THREADS = 128;
 constexpr int CONV_ROWS = 64;
+constexpr int CONV_G_BF16 = 8;  // bf16 rows in flight per thread
 
 // First run slot of stream s.
 __device__ __forceinline__ int conv_run_base(const int32_t *cu, int s) {
@@ -174,24 +175,21 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 
     const T *xp = x + (int64_t)r0 * xs + c0;
     T *op = out + (int64_t)r0 * os + c0;
-    // rows in groups of 6: the 6 loads are issued before any of them is used (6 keeps the
-    // kernel at 8 blocks of 128 threads per SM; 8 would need more registers than that allows)
-    constexpr int G = 6;
+    // rows in groups of G: the G loads are issued before any of them is used, and held as
+    // loaded (bf16: two registers a row) until their row is computed, so that more rows are in
+    // flight within the 64 registers that 8 blocks of 128 threads per SM allow
+    constexpr int G = sizeof(T) == 2 ? CONV_G_BF16 : 6;
     for (int g0 = r0; g0 < r1; g0 += G, xp += G * xs, op += G * os) {
-        float cur[G][N];
+        typename V::Raw raw[G];
+#pragma unroll
+        for (int q = 0; q < G; ++q)
+            raw[q] = (active && g0 + q < r1) ? V::load_raw(xp + q * xs) : V::zero_raw();
 #pragma unroll
         for (int q = 0; q < G; ++q) {
-            if (active && g0 + q < r1) {
-                V::load(xp + q * xs, cur[q]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < N; ++e) cur[q][e] = 0.f;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < G; ++q) {
+            float cur[N];
+            V::widen(raw[q], cur);
             float y[N];
-            conv_row<T, K, HD>(wp, bp, win, cur[q], l2_warp, do_l2, eps, y);
+            conv_row<T, K, HD>(wp, bp, win, cur, l2_warp, do_l2, eps, y);
             if (active && g0 + q < r1) V::store(op + q * os, y);
             if constexpr (K > 1) {
 #pragma unroll
@@ -199,7 +197,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
 #pragma unroll
                     for (int e = 0; e < N; ++e) win[m][e] = win[m + 1][e];
 #pragma unroll
-                for (int e = 0; e < N; ++e) win[K - 2][e] = cur[q][e];
+                for (int e = 0; e < N; ++e) win[K - 2][e] = cur[e];
             }
         }
     }
