@@ -3,13 +3,15 @@
 
 One step = one pass of the whole hot path over one packed batch that is already resident in
 HBM: conv1d + SiLU (carried conv state) -> L2 over the q|k heads -> chunked gated delta rule,
-all through the C ABI. Default workload: GDN batched, 8 streams x 2048 tokens, 16 heads,
-head dim 128, bf16 activations, fp32 states.
+all through the C ABI. Default workload: the largest one, KDA varlen, 64 streams with
+log-uniform lengths in [16, 16384] summing to 262144 tokens, 32 heads, head dim 128, bf16
+activations, fp32 states, with the conv1d + SiLU + L2 front end.
 
 Prints ONE JSON line (rank 0). `--impl reference` times the fp64 CPU oracle instead (the
 reference arm of this path), on bounded samples of the same workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                       [--streams S]   (profiling slices: the first S streams of the workload)
 Multi-GPU (replicas, weak scaling): torchrun --nproc-per-node N bench.py --gpus N ...
 """
 from __future__ import annotations
@@ -34,7 +36,7 @@ import torch  # noqa: E402
 from linear_attention_chunked_conv1d_gb300.inputs import (  # noqa: E402
     DECODE_WORKLOADS, PROJ_WORKLOADS, WORKLOADS, make_inputs)
 
-DEFAULT_WORKLOAD = "gdn_batched_8x2048_h16_d128"
+DEFAULT_WORKLOAD = "kda_varlen_64_h32_d128"
 METRIC = "prefill tokens/s per GDN/KDA layer"
 DECODE_METRIC = "decode tokens/s per GDN/KDA layer"
 PROJ_METRIC = "phase-1 projection tokens/s (QKVZ GEMM)"
@@ -205,15 +207,13 @@ def stream_cpu(inp, s, conv_w):
             f(inp["beta"][a:b]), b - a, conv_w)
 
 
-def cpu_baseline(wl, inp, budget_s=12.0):
-    """Time the oracle on whole streams of the workload until about budget_s of CPU work."""
-    import oracle
-    oracle.build()
-    threads = os.cpu_count() or 1
-    conv_w = inp["conv_w"].detach().to("cpu", torch.float64).numpy()
+# Workloads whose oracle time is also reported on one host thread (the two small GDN ones).
+SINGLE_THREAD_BASELINE = ("gdn_t100_h4_d64_f32", "gdn_batched_8x2048_h16_d128")
+
+
+def _oracle_over_streams(wl, inp, conv_w, threads, budget_s):
     done_tokens, elapsed, streams = 0, 0.0, 0
-    order = list(range(wl.B))
-    for s in order:
+    for s in range(wl.B):
         data = stream_cpu(inp, s, conv_w)
         t0 = time.perf_counter()
         oracle_sample(wl, data, threads)
@@ -222,10 +222,28 @@ def cpu_baseline(wl, inp, budget_s=12.0):
         streams += 1
         if elapsed >= budget_s:
             break
-    return {"value": done_tokens / elapsed, "unit": "tokens/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{streams} of {wl.B} streams ({done_tokens} tokens, all {wl.Hv} v-heads): "
-                      f"fp64 conv1d+SiLU -> L2 -> token-by-token recurrence, {elapsed:.1f} s"}
+    return done_tokens, elapsed, streams
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """Time the oracle on whole streams of the workload until about budget_s of CPU work, on
+    every host core; for the two small GDN workloads also on one thread."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    conv_w = inp["conv_w"].detach().to("cpu", torch.float64).numpy()
+    done_tokens, elapsed, streams = _oracle_over_streams(wl, inp, conv_w, threads, budget_s)
+    res = {"value": done_tokens / elapsed, "unit": "tokens/s", "cores": threads,
+           "kind": "oracle",
+           "sample": f"{streams} of {wl.B} streams ({done_tokens} tokens, all {wl.Hv} v-heads): "
+                     f"fp64 conv1d+SiLU -> L2 -> token-by-token recurrence, {elapsed:.1f} s"}
+    if wl.name in SINGLE_THREAD_BASELINE:
+        t1, e1, s1 = _oracle_over_streams(wl, inp, conv_w, 1, budget_s / 2)
+        res["single_thread"] = {
+            "value": t1 / e1, "unit": "tokens/s", "cores": 1,
+            "sample": f"{s1} of {wl.B} streams ({t1} tokens, all {wl.Hv} v-heads) on one "
+                      f"host thread, {e1:.1f} s"}
+    return res
 
 
 def run_reference_proj(args, wl):
@@ -251,7 +269,7 @@ def run_reference_proj(args, wl):
         "impl": "reference", "metric": PROJ_METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe in DESIGN.md)",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; x~N(0,1), conv w~N(0,0.25), h~N(0,0.02), g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
         "config": {"workload": wl.name, "hidden": Kd, "outputs": N},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"each step: {rows} of the stacked rows against the full "
@@ -292,7 +310,7 @@ def run_reference(args, wl):
         "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe in DESIGN.md)",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; x~N(0,1), conv w~N(0,0.25), h~N(0,0.02), g=-softplus(N(0,1)), beta=sigmoid(N(0,1)))",
         "config": {"workload": wl.name, "streams": wl.B, "Hk": wl.Hk, "Hv": wl.Hv,
                    "head_dim": wl.d, "variant": wl.variant, "activations": wl.dtype},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
@@ -319,6 +337,17 @@ def aggregate(tokens_local: int, ms_local: float, pg=None, device=None):
     return float(n.item()) / (ms * 1e-3), ms, pg.get_world_size()
 
 
+def stream_slice(wl, n):
+    """The workload restricted to its first n streams: lengths drawn as for the whole workload
+    (same seed), the other inputs drawn afresh for these streams only (same distributions)."""
+    from linear_attention_chunked_conv1d_gb300.inputs import draw_lengths
+    gen = torch.Generator("cpu")
+    gen.manual_seed(0)
+    lengths = draw_lengths(wl, gen)[:n]
+    return wl.replace(name=f"{wl.name}[streams 0..{n - 1}]", B=n,
+                      lengths="list:" + ",".join(str(v) for v in lengths))
+
+
 def uses_tensor_cores(wl) -> bool:
     return wl.dtype == "bf16" and wl.d == 128
 
@@ -332,9 +361,14 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(ALL_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--streams", type=int, default=0,
+                    help="profiling slice: keep only the first S streams of the workload (their "
+                         "lengths as drawn for the whole workload)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = ALL_WORKLOADS[args.workload]
+    if args.streams and wl.mode == "prefill" and args.streams < wl.B:
+        wl = stream_slice(wl, args.streams)
     if args.impl == "reference":
         run_reference(args, wl)
         return

@@ -16,7 +16,18 @@
  * Conventions shared by every call
  *  - Pointers are raw DEVICE pointers owned by the caller, unless stated otherwise. The library
  *    allocates no device memory and keeps no per-call state; all work is enqueued on `stream`
- *    (a cudaStream_t passed as uint64_t; 0 = legacy default stream) and is asynchronous.
+ *    (a cudaStream_t passed as uint64_t; 0 = legacy default stream) and is asynchronous. Two
+ *    fixed arrays live in the library's own device image for the life of the process: the
+ *    status word of la_device_status and the scratch of la_gdn_prefill_varlen_noalloc. Their
+ *    device addresses are looked up once per device and cached, so a cudaDeviceReset (or any
+ *    other teardown of the primary context) invalidates them: do not call the library on a
+ *    device after resetting it in the same process.
+ *  - Host-side fault injection (testing): with the environment variable LA_FAULT_INJECT set to
+ *    "launch", every call that passes its checks returns LA_ERR_CUDA ("injected launch
+ *    failure") instead of launching; set to "alloc", every call that needs one of the library's
+ *    device arrays (the status word, the no-allocation scratch) returns LA_ERR_CUDA as if its
+ *    address lookup had failed. Nothing is launched and no buffer is touched in either case.
+ *    The variable is read at every call.
  *  - Every check runs on the host BEFORE any launch; on error nothing is launched and no buffer
  *    is touched. Return value: LA_OK or one of the LA_ERR_* codes; la_last_error() then gives a
  *    thread-local message.
@@ -60,6 +71,12 @@ extern "C" {
 #define LA_DEV_BAD_SEQLENS 1 /* cu_seqlens not monotone, out of range, or a length > max_seqlen */
 #define LA_DEV_TIMEOUT 2     /* a bounded wait inside a kernel gave up; that kernel's results are
                                 incomplete (never expected; reported instead of hanging) */
+/* Every wait of the tensor-core kernels on an mbarrier (MMA or copy completion) gives up after
+ * 2 s; the block then drains its own MMAs and copies, frees its tensor memory, raises
+ * LA_DEV_TIMEOUT and exits, so the context stays usable. Two environment variables, read at
+ * every call, exist to test that path: LA_WAIT_LIMIT_NS (a positive integer) replaces the 2 s
+ * limit, and LA_DEBUG_STALL=1 makes each block of those kernels wait once on a barrier that
+ * nothing completes, so that the wait runs out. Neither is meant for production use. */
 
 /* ABI version of this header (bumped on any signature change). */
 #define LA_ABI_VERSION 1

@@ -27,7 +27,7 @@ __all__ = [
 
 LA_OK, LA_ERR_ARG, LA_ERR_COUNT, LA_ERR_UNSUPPORTED, LA_ERR_CUDA = 0, 1, 2, 3, 4
 LA_F32, LA_BF16 = 0, 1
-LA_DEV_BAD_SEQLENS = 1
+LA_DEV_BAD_SEQLENS, LA_DEV_TIMEOUT = 1, 2
 _CODES = {LA_ERR_ARG: "LA_ERR_ARG", LA_ERR_COUNT: "LA_ERR_COUNT",
           LA_ERR_UNSUPPORTED: "LA_ERR_UNSUPPORTED", LA_ERR_CUDA: "LA_ERR_CUDA"}
 
@@ -238,7 +238,11 @@ def gdn_prefill_varlen_noalloc(h_state_ptrs, q, k, v, g, beta, out, cu_seqlens, 
     """gdn_prefill_varlen without a workspace, for callers that cannot allocate device memory:
     the library's fixed scratch (up to 4096 streams per call) is used instead. Calls that
     overlap on the GPU share that scratch and must be ordered; the first call on a device
-    should come before any stream capture there."""
+    should come before any stream capture there. The entry point is compiled for bf16 q, k, v
+    and out only: any other dtype is refused here (the C call has no dtype argument)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"gdn_prefill_varlen_noalloc takes bf16 tensors; {name} is {t.dtype}")
     B = cu_seqlens.shape[0] - 1
     total = q.shape[0] if total_tokens is None else total_tokens
     scale = 1.0 / math.sqrt(dk) if scale is None else scale

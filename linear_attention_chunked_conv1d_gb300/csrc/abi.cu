@@ -7,6 +7,8 @@
 // instances.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -36,7 +38,21 @@ constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices];
 std::once_flag g_status_once[kMaxDevices];
 
+// Host-side fault injection for tests: LA_FAULT_INJECT=launch makes every call that passed
+// its checks return LA_ERR_CUDA instead of launching; LA_FAULT_INJECT=alloc makes the lookup
+// of the library's device arrays fail. Read at every call, so a test can switch it on and off.
+enum Inject { INJECT_NONE = 0, INJECT_LAUNCH = 1, INJECT_ALLOC = 2 };
+
+Inject fault_inject() {
+    const char *v = getenv("LA_FAULT_INJECT");
+    if (!v) return INJECT_NONE;
+    if (!strcmp(v, "launch")) return INJECT_LAUNCH;
+    if (!strcmp(v, "alloc")) return INJECT_ALLOC;
+    return INJECT_NONE;
+}
+
 int *status_ptr() {
+    if (fault_inject() == INJECT_ALLOC) return nullptr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::call_once(g_status_once[dev], [dev] {
@@ -44,6 +60,33 @@ int *status_ptr() {
         if (cudaGetSymbolAddress(&p, g_dev_status) == cudaSuccess) g_status_ptr[dev] = (int *)p;
     });
     return g_status_ptr[dev];
+}
+
+// The status word of the current device, or LA_ERR_CUDA when its address cannot be had. Every
+// launching call takes it right before its launch, so an injected launch failure is reported
+// here already (before any CUDA call).
+int get_status(int **out) {
+    *out = nullptr;
+    if (fault_inject() == INJECT_LAUNCH)
+        return fail(LA_ERR_CUDA, "injected launch failure (LA_FAULT_INJECT=launch)");
+    *out = status_ptr();
+    if (!*out)
+        return fail(LA_ERR_CUDA, fault_inject() == INJECT_ALLOC
+                                     ? "injected allocation failure (LA_FAULT_INJECT=alloc)"
+                                     : "the device status word could not be looked up");
+    return LA_OK;
+}
+
+// Limit of the bounded waits inside the tensor-core kernels: 2 s, or LA_WAIT_LIMIT_NS (a test
+// knob that lets a wait run out on purpose; read at every call).
+uint64_t wait_limit_ns() {
+    const char *v = getenv("LA_WAIT_LIMIT_NS");
+    if (v && *v) {
+        char *end = nullptr;
+        const unsigned long long n = strtoull(v, &end, 10);
+        if (end && *end == '\0' && n > 0) return (uint64_t)n;
+    }
+    return 2000000000ull;
 }
 
 cudaStream_t as_stream(uint64_t s) { return reinterpret_cast<cudaStream_t>(static_cast<uintptr_t>(s)); }
@@ -73,7 +116,12 @@ int check_stride(int64_t stride, int64_t width, int dtype, const char *name) {
     return LA_OK;
 }
 
-int launch_result(cudaError_t e, const char *what) {
+// Runs a launch (a callable returning cudaError_t) unless a launch failure is injected.
+template <class F>
+int launch_result(F &&launch, const char *what) {
+    if (fault_inject() == INJECT_LAUNCH)
+        return fail(LA_ERR_CUDA, "%s: injected launch failure (LA_FAULT_INJECT=launch)", what);
+    const cudaError_t e = launch();
     if (e != cudaSuccess) return fail(LA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
     return ok();
 }
@@ -138,11 +186,20 @@ bool uses_tensor_cores(int dtype, int dk, int dv) {
     return la::chunk_tc_supported(a);
 }
 
+// Test knob LA_DEBUG_STALL=1: the tensor-core kernels make one wait on a barrier that nothing
+// completes, which runs out after the wait limit (read at every call).
+int debug_stall() {
+    const char *v = getenv("LA_DEBUG_STALL");
+    return v && !strcmp(v, "1") ? 1 : 0;
+}
+
 int run_recurrence(la::RecArgs &a, cudaStream_t st) {
-    a.status = status_ptr();
+    LA_TRY(get_status(&a.status));
+    a.wait_ns = wait_limit_ns();
+    a.debug_stall = debug_stall();
     if (la::chunk_tc_supported(a))
-        return launch_result(la::launch_chunk_tc(a, st), "chunked recurrence (tcgen05) launch");
-    return launch_result(la::launch_chunk_simt(a, st), "chunked recurrence launch");
+        return launch_result([&] { return la::launch_chunk_tc(a, st); }, "chunked recurrence (tcgen05) launch");
+    return launch_result([&] { return la::launch_chunk_simt(a, st); }, "chunked recurrence launch");
 }
 
 }  // namespace
@@ -176,8 +233,8 @@ int la_conv1d_silu_prefill(void *conv_state, const void *x, const void *w, const
     a.x = x; a.w = w; a.bias = bias; a.out = out;
     a.cu = nullptr; a.B = 1; a.total = t; a.channels = channels; a.kernel = kernel;
     a.x_stride = x_stride; a.out_stride = out_stride; a.dtype = dtype;
-    a.status = status_ptr();
-    return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu launch");
+    LA_TRY(get_status(&a.status));
+    return launch_result([&] { return la::launch_conv1d_silu(a, as_stream(stream)); }, "conv1d_silu launch");
 }
 
 int la_conv1d_silu_prefill_varlen(const uint64_t *conv_state_ptrs, const void *x, const void *w,
@@ -197,8 +254,8 @@ int la_conv1d_silu_prefill_varlen(const uint64_t *conv_state_ptrs, const void *x
     a.x = x; a.w = w; a.bias = bias; a.out = out;
     a.cu = cu_seqlens; a.B = B; a.total = total_tokens; a.channels = channels; a.kernel = kernel;
     a.x_stride = x_stride; a.out_stride = out_stride; a.dtype = dtype;
-    a.status = status_ptr();
-    return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu launch");
+    LA_TRY(get_status(&a.status));
+    return launch_result([&] { return la::launch_conv1d_silu(a, as_stream(stream)); }, "conv1d_silu launch");
 }
 
 int la_conv1d_silu_l2_prefill(const uint64_t *conv_state_ptrs, const void *x, const void *w,
@@ -225,8 +282,8 @@ int la_conv1d_silu_l2_prefill(const uint64_t *conv_state_ptrs, const void *x, co
     a.cu = cu_seqlens; a.B = B; a.total = total_tokens; a.channels = channels; a.kernel = kernel;
     a.x_stride = x_stride; a.out_stride = out_stride; a.dtype = dtype;
     a.l2_heads = l2_heads; a.head_dim = head_dim; a.eps = eps;
-    a.status = status_ptr();
-    return launch_result(la::launch_conv1d_silu(a, as_stream(stream)), "conv1d_silu_l2 launch");
+    LA_TRY(get_status(&a.status));
+    return launch_result([&] { return la::launch_conv1d_silu(a, as_stream(stream)); }, "conv1d_silu_l2 launch");
 }
 
 int la_l2norm_heads(void *x, int t, int n_heads, int head_dim, int64_t row_stride, float eps,
@@ -240,7 +297,7 @@ int la_l2norm_heads(void *x, int t, int n_heads, int head_dim, int64_t row_strid
     LA_TRY(check_stride(row_stride, (int64_t)n_heads * head_dim, dtype, "row_stride"));
     if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
     la::L2Args a{x, t, n_heads, head_dim, row_stride, eps, dtype};
-    return launch_result(la::launch_l2norm_heads(a, as_stream(stream)), "l2norm launch");
+    return launch_result([&] { return la::launch_l2norm_heads(a, as_stream(stream)); }, "l2norm launch");
 }
 
 size_t la_prefill_workspace_bytes(int B, int total_tokens, int Hk, int Hv, int dk, int dv,
@@ -321,6 +378,11 @@ int la_gdn_prefill_varlen_noalloc(const uint64_t *h_state_ptrs, const void *q, c
                     "la_gdn_prefill_varlen with a caller workspace", B, max_streams);
     LA_TRY(rec_common(h_state_ptrs, q, k, v, g, beta, out, B, Hk, Hv, dk, dv, q_stride, k_stride,
                       v_stride, LA_BF16, nullptr, 0, 0));
+    if (fault_inject() == INJECT_LAUNCH)
+        return fail(LA_ERR_CUDA, "injected launch failure (LA_FAULT_INJECT=launch)");
+    if (fault_inject() == INJECT_ALLOC)
+        return fail(LA_ERR_CUDA, "looking up the fixed scratch: injected allocation failure "
+                                 "(LA_FAULT_INJECT=alloc)");
     void *scratch = nullptr;
     size_t scratch_bytes = 0;
     cudaError_t e = la::chunk_tc_static_scratch(&scratch, &scratch_bytes);
@@ -432,8 +494,10 @@ int la_prefill_front(const uint64_t *conv_state_ptrs, const uint64_t *h_state_pt
     a.x = x; a.conv_w = conv_w; a.conv_bias = conv_bias; a.conv_state_ptrs = conv_state_ptrs;
     a.x_stride = x_stride; a.conv_k = conv_kernel; a.l2_eps = l2_eps;
     a.z = z; a.norm_w = z ? norm_w : nullptr; a.norm_eps = norm_eps;
-    a.status = status_ptr();
-    return launch_result(la::launch_chunk_tc(a, as_stream(stream)), "fused prefill (tcgen05) launch");
+    LA_TRY(get_status(&a.status));
+    a.wait_ns = wait_limit_ns();
+    a.debug_stall = debug_stall();
+    return launch_result([&] { return la::launch_chunk_tc(a, as_stream(stream)); }, "fused prefill (tcgen05) launch");
 }
 
 int la_gated_rmsnorm(const void *o, const void *z, const void *w, void *y, int t, int Hv, int dv,
@@ -450,7 +514,7 @@ int la_gated_rmsnorm(const void *o, const void *z, const void *w, void *y, int t
     if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
     if (y == z) return fail(LA_ERR_ARG, "y may not alias z");
     la::GatedNormArgs a{o, z, w, y, t, Hv, dv, eps, dtype};
-    return launch_result(la::launch_gated_rmsnorm(a, as_stream(stream)), "gated rmsnorm launch");
+    return launch_result([&] { return la::launch_gated_rmsnorm(a, as_stream(stream)); }, "gated rmsnorm launch");
 }
 
 size_t la_decode_workspace_bytes(int B, int Hk, int Hv, int dk, int dv, int dtype) {
@@ -496,7 +560,8 @@ int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs
     if (!workspace || !aligned16(workspace))
         return fail(LA_ERR_ARG, "workspace is NULL or not 16-byte aligned");
     const int64_t row = (int64_t)(need / (size_t)B) / (dtype == LA_BF16 ? 2 : 4);  // elements
-    int *status = status_ptr();
+    int *status = nullptr;
+    LA_TRY(get_status(&status));
     la::ConvArgs c{};
     c.state_ptrs = conv_state_ptrs;
     c.x = x; c.w = conv_w; c.bias = conv_bias; c.out = workspace;
@@ -506,13 +571,12 @@ int la_decode_step(const uint64_t *conv_state_ptrs, const uint64_t *h_state_ptrs
     c.status = status;
     c.one_per_stream = true;
     cudaStream_t st = as_stream(stream);
-    cudaError_t e = la::launch_conv1d_silu(c, st);
-    if (e != cudaSuccess) return launch_result(e, "decode front end launch");
+    LA_TRY(launch_result([&] { return la::launch_conv1d_silu(c, st); }, "decode front end launch"));
     la::DecArgs d{};
     d.h_ptrs = h_state_ptrs; d.qkv = workspace; d.qkv_stride = row;
     d.g = g; d.beta = beta; d.out = out;
     d.B = B; d.Hk = Hk; d.Hv = Hv; d.d = dk; d.scale = scale; d.dtype = dtype; d.kda = kda == 1;
-    return launch_result(la::launch_decode_recurrence(d, st), "decode recurrence launch");
+    return launch_result([&] { return la::launch_decode_recurrence(d, st); }, "decode recurrence launch");
 }
 
 int la_gemm_bf16(const void *a, const void *w, void *c, int M, int N, int K, int64_t lda,
@@ -532,8 +596,10 @@ int la_gemm_bf16(const void *a, const void *w, void *c, int M, int N, int K, int
     };
     if (overlaps(a, M, lda, K) || overlaps(w, N, ldw, K))
         return fail(LA_ERR_ARG, "c may not overlap a or w");
-    la::GemmArgs g{a, w, c, M, N, K, lda, ldw, ldc, status_ptr()};
-    return launch_result(la::launch_gemm_bf16(g, as_stream(stream)), "gemm (tcgen05) launch");
+    int *status = nullptr;
+    LA_TRY(get_status(&status));
+    la::GemmArgs g{a, w, c, M, N, K, lda, ldw, ldc, status, wait_limit_ns(), debug_stall()};
+    return launch_result([&] { return la::launch_gemm_bf16(g, as_stream(stream)); }, "gemm (tcgen05) launch");
 }
 
 int la_rmsnorm_rows(const void *x, const void *w, void *y, int rows, int width, int64_t ldx,
@@ -549,7 +615,7 @@ int la_rmsnorm_rows(const void *x, const void *w, void *y, int rows, int width, 
     LA_TRY(check_stride(ldy, width, LA_BF16, "ldy"));
     if (!(eps >= 0.f)) return fail(LA_ERR_ARG, "eps must be >= 0");
     la::RowNormArgs a{x, w, y, rows, width, ldx, ldy, eps};
-    return launch_result(la::launch_rmsnorm_rows(a, as_stream(stream)), "rmsnorm launch");
+    return launch_result([&] { return la::launch_rmsnorm_rows(a, as_stream(stream)); }, "rmsnorm launch");
 }
 
 int la_gate_activations(const void *ab, int64_t ld, int t, int na, int nb, float *g,
@@ -559,7 +625,7 @@ int la_gate_activations(const void *ab, int64_t ld, int t, int na, int nb, float
     if (!ab || !g || !beta) return fail(LA_ERR_ARG, "ab, g and beta must not be NULL");
     if (ld < (int64_t)na + nb) return fail(LA_ERR_ARG, "ld (%lld) is below na + nb", (long long)ld);
     la::GateArgs a{ab, ld, t, na, nb, g, beta};
-    return launch_result(la::launch_gate_activations(a, as_stream(stream)), "gate activations launch");
+    return launch_result([&] { return la::launch_gate_activations(a, as_stream(stream)); }, "gate activations launch");
 }
 
 size_t la_prefill_segmented_workspace_bytes(int total_tokens, int Hv, int segments) {
@@ -593,8 +659,9 @@ int la_prefill_segmented(const uint64_t *h_state_ptrs, const void *q, const void
     a.q_stride = q_stride; a.k_stride = k_stride; a.v_stride = v_stride;
     a.scale = scale; a.pad_fill = 0.f; a.dtype = dtype; a.kda = kda == 1;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
-    a.status = status_ptr();
-    return launch_result(la::launch_segmented(a, segments, as_stream(stream)), "segmented scan launch");
+    LA_TRY(get_status(&a.status));
+    a.wait_ns = wait_limit_ns();
+    return launch_result([&] { return la::launch_segmented(a, segments, as_stream(stream)); }, "segmented scan launch");
 }
 
 }  // extern "C"

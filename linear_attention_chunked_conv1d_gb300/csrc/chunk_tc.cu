@@ -342,10 +342,11 @@ __device__ __forceinline__ void write_conv_state(const RecArgs &a, const unsigne
     }
 }
 
-// Block-wide barrier that also reports whether any thread raised the local error flag.
+// Block-wide barrier that also reports whether any thread raised the local error flag. The
+// answer is the OR of every thread's own reading, so all threads take the same branch even if a
+// thread raises the flag again right after the barrier.
 __device__ __forceinline__ bool sync_ok(volatile int *flag) {
-    __syncthreads();
-    return *flag == 0;
+    return __syncthreads_or(*flag) == 0;
 }
 
 template <bool KDA, bool FRONT>
@@ -361,6 +362,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     uint64_t *bar_b = bar_a + 1;
     uint64_t *bar_c = reinterpret_cast<uint64_t *>(sm + SM_BARS + 40);  // state update done
     uint64_t *bar_d = reinterpret_cast<uint64_t *>(sm + SM_BARS + 48);  // block-substitution steps
+    uint64_t *bar_e = reinterpret_cast<uint64_t *>(sm + SM_BARS + 56);  // final drain of the MMAs
     volatile int *err = reinterpret_cast<volatile int *>(sm + SM_BARS + 16);
     volatile int *unit_sh = err + 1;
     volatile int *slow_sh = err + 2;
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         tc::mbar_init(bar_b, 1);
         tc::mbar_init(bar_c, 1);
         tc::mbar_init(bar_d, 1);
+        tc::mbar_init(bar_e, 1);
         tc::fence_mbar_init();
     }
     // identity tile (bf16, K-major 64x64) for the transposing MMAs
@@ -403,8 +406,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     uint32_t phase_a = 0, phase_b = 0, phase_c = 0;
     bool pend_c = false;  // a state-update MMA group not yet waited for
 
+    const uint64_t wait_ns = a.wait_ns ? a.wait_ns : WAIT_NS;
     auto wait_bar = [&](uint64_t *bar, uint32_t &ph) {
-        const bool ok = tc::mbar_wait(bar, ph, WAIT_NS);
+        const bool ok = tc::mbar_wait(bar, ph, wait_ns);
         ph ^= 1u;
         if (!ok) *err = 1;
         tc::fence_after_sync();
@@ -433,9 +437,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     for (;;) {
         __syncthreads();  // everyone has read the previous unit index
         if (tid == 0) *unit_sh = atomicAdd(P.counter, 1);
-        __syncthreads();
+        if (!sync_ok(err)) break;
         const int u = *unit_sh;
-        if (u >= P.num_units || *err) break;
+        if (u >= P.num_units) break;
         const int s = P.perm[u / Hv];
         const int j = u % Hv;
         const int kh = j / group;
@@ -577,6 +581,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
             cp_async_wait_all();
             tc::fence_async_smem();
+            if (a.debug_stall) {  // test knob: a wait on a barrier nothing completes runs out
+                uint32_t never = 0;
+                wait_bar(bar_e, never);
+            }
             if (!sync_ok(err)) break;
             // this chunk's scalar gates are in shared memory: fetch the next chunk's
             if (!last) fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
@@ -994,7 +1002,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8,
                                     tc::sdesc_sw128((sb + SM_T00) + kk * 32u), id32, kk > 0);
                 tc::mma_commit(bar_d);
-                ok = tc::mbar_wait(bar_d, 0, WAIT_NS);
+                ok = tc::mbar_wait(bar_d, 0, wait_ns);
                 tc::fence_after_sync();
                 if (ok) {
 #pragma unroll
@@ -1002,7 +1010,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                         tc::mma_tf32_ts(tm + COL_D6 + 32, tm + COL_D6 + kk * 8,
                                         tc::sdesc_sw128((sb + SM_NA10) + kk * 32u), id32, 1);
                     tc::mma_commit(bar_d);
-                    ok = tc::mbar_wait(bar_d, 1, WAIT_NS);
+                    ok = tc::mbar_wait(bar_d, 1, wait_ns);
                     tc::fence_after_sync();
                 }
                 if (ok) {
@@ -1119,14 +1127,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             __syncthreads();
             tc::fence_after_sync();
         }
-        if (*err) break;
+        if (!sync_ok(err)) break;
         if (pend_n > 0) {  // the last chunk's output (staged before the barrier above)
             store_o(pend_tok0, pend_n);
             pend_n = 0;
         }
 
         wait_state();
-        if (*err) break;
+        if (!sync_ok(err)) break;
         // state back: H[c][d] = S[d][c]
 #pragma unroll
         for (int g = 0; g < D32 / 16; ++g) {
@@ -1142,10 +1150,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     }
 
     cp_async_wait_all();
-    if (pend_c) tc::mbar_wait(bar_c, phase_c, WAIT_NS);  // after an error: no MMA left in flight
-    if (*err && tid == 0) raise_status(a.status, LA_DEV_TIMEOUT);
+    // Every MMA of this block has completed before its TMEM is released, also after a wait gave
+    // up: the issuing lane commits once more (a commit tracks all earlier MMAs of its thread)
+    // and waits for that commit with the full limit.
+    if (warp == 0) {
+        __syncwarp();
+        if (tc::elect_one()) {
+            tc::mma_commit(bar_e);
+            if (!tc::mbar_wait(bar_e, 0, WAIT_NS)) *err = 1;
+        }
+        __syncwarp();
+    }
     tc::fence_before_sync();
     __syncthreads();
+    if (*err && tid == 0) raise_status(a.status, LA_DEV_TIMEOUT);
     if (warp == 0) tc::tmem_dealloc(tm, TMEM_COLS);
 }
 

@@ -58,7 +58,8 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 
 __global__ void __launch_bounds__(G_THREADS, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
-                 __nv_bfloat16 *__restrict__ C, int M, int N, int K, int64_t ldc, int *status) {
+                 __nv_bfloat16 *__restrict__ C, int M, int N, int K, int64_t ldc, int *status,
+                 uint64_t wait_ns, int debug_stall) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -104,7 +105,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 const int m0 = (tile / nt) * GM, n0 = (tile % nt) * GN;
                 for (int k = 0; k < kb; ++k, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!tc::mbar_wait(empty + s, ph ^ 1u, G_WAIT_NS) || *err) {
+                    if (!tc::mbar_wait(empty + s, ph ^ 1u, wait_ns) || *err) {
                         *err = 1;
                         break;
                     }
@@ -124,9 +125,12 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         if (tc::elect_one()) {  // ---- MMA issuer
             constexpr uint32_t id = tc::idesc(GM, GN, tc::FMT_BF16);
             uint32_t it = 0, tcnt = 0;
+            // test knob: a wait on a barrier nothing has completed yet (its first phase ends
+            // with the final commit below) runs out, and the block unwinds
+            if (debug_stall && !tc::mbar_wait(fin, 0, wait_ns)) *err = 1;
             for (int tile = blockIdx.x; tile < ntiles && !*err; tile += gridDim.x, ++tcnt) {
                 const uint32_t acc = tcnt & 1u, aph = (tcnt >> 1) & 1u;
-                if (!tc::mbar_wait(acce + acc, aph ^ 1u, G_WAIT_NS)) {
+                if (!tc::mbar_wait(acce + acc, aph ^ 1u, wait_ns)) {
                     *err = 1;
                     break;
                 }
@@ -135,7 +139,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 bool ok = true;
                 for (int k = 0; k < kb; ++k, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!tc::mbar_wait(full + s, ph, G_WAIT_NS) || *err) {
+                    if (!tc::mbar_wait(full + s, ph, wait_ns) || *err) {
                         ok = false;
                         break;
                     }
@@ -160,9 +164,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     } else {  // ---- epilogue: warps 2-5, TMEM lane quadrant warp % 4
         const uint32_t q = warp & 3;
         uint32_t tcnt = 0;
-        for (int tile = blockIdx.x; tile < ntiles && !*err; tile += gridDim.x, ++tcnt) {
+        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tcnt) {
+            // every decision to stop is made per warp: the TMEM loads below are warp-collective
+            if (__any_sync(0xffffffffu, *err != 0)) break;
             const uint32_t acc = tcnt & 1u, aph = (tcnt >> 1) & 1u;
-            if (!tc::mbar_wait(accf + acc, aph, G_WAIT_NS)) {
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(accf + acc, aph, wait_ns))) {
                 *err = 1;
                 break;
             }
@@ -216,7 +222,9 @@ cudaError_t launch_gemm_bf16(const GemmArgs &a, cudaStream_t st) {
                                          (int)G_SMEM);
     if (e != cudaSuccess) return e;
     gemm_bf16_kernel<<<grid, G_THREADS, G_SMEM, st>>>(ma, mw, reinterpret_cast<__nv_bfloat16 *>(a.c),
-                                                      a.M, a.N, a.K, a.ldc, a.status);
+                                                      a.M, a.N, a.K, a.ldc, a.status,
+                                                      a.wait_ns ? a.wait_ns : G_WAIT_NS,
+                                                      a.debug_stall);
     return cudaGetLastError();
 }
 

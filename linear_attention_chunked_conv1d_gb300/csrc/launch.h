@@ -47,6 +47,8 @@ struct RecArgs {
     void *workspace;
     size_t workspace_bytes;
     int *status;
+    uint64_t wait_ns;  // tensor-core kernel: limit of its bounded waits (0: the 2 s default)
+    int debug_stall;   // tensor-core kernel, test knob: one wait on a barrier nothing completes
     // Fused front end (tensor-core kernel only): q, k and v are not read; each block computes
     // them per chunk from the pre-conv rows x [tok][cd] (cd = 2 Hk dk + Hv dv, packed
     // q | k | v heads), the depthwise conv weights [cd][conv_k] (+ optional bias [cd]) and
@@ -117,6 +119,8 @@ struct GemmArgs {
     int M, N, K;
     int64_t lda, ldw, ldc;
     int *status;
+    uint64_t wait_ns;  // limit of the kernel's bounded waits (0: the 2 s default)
+    int debug_stall;   // test knob: one wait on a barrier that nothing completes
 };
 cudaError_t launch_gemm_bf16(const GemmArgs &a, cudaStream_t st);
 

@@ -1,5 +1,5 @@
-// Host-side TMA tensor-map encoding shared by the kernels that load tiles with
-// cp.async.bulk.tensor (the projection GEMM and the conv front end).
+// Host-side TMA tensor-map encoding for the kernels that load tiles with
+// cp.async.bulk.tensor (the projection GEMM).
 #include <cuda.h>
 
 #include <mutex>

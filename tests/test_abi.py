@@ -264,3 +264,77 @@ def test_segmented_refusals(lib):
     assert rc(dk=64, dv=64) == lib.LA_ERR_UNSUPPORTED
     assert rc(wsb=100) == lib.LA_ERR_ARG
     assert L.la_prefill_segmented_workspace_bytes(4096, 32, 2) > 32 * 128 * 128 * 4 * 3
+
+
+# ---------------------------------------------------------------- host-side fault injection
+@pytest.fixture
+def inject(monkeypatch):
+    """Sets LA_FAULT_INJECT for one test (the library reads it at every call)."""
+    def set_(mode):
+        if mode is None:
+            monkeypatch.delenv("LA_FAULT_INJECT", raising=False)
+        else:
+            monkeypatch.setenv("LA_FAULT_INJECT", mode)
+    yield set_
+    monkeypatch.delenv("LA_FAULT_INJECT", raising=False)
+
+
+def _valid_calls(lib):
+    """One call per launching entry point with arguments that pass every host check (fake,
+    aligned addresses: with a fault injected the call returns before any CUDA call)."""
+    L = lib._load()
+    ws = 1 << 20
+    return {
+        "conv": lambda: _rc_conv(lib, 5, 10),
+        "l2": lambda: L.la_l2norm_heads(A, 4, 2, 128, 256, 1e-6, 1, 0),
+        "gdn_batched": lambda: _rc_gdn_batched(lib, 2, 8, 100, ws=A * 64, wsb=ws),
+        "gdn_varlen_noalloc": lambda: L.la_gdn_prefill_varlen_noalloc(
+            A, A, A, A, A, A, A * 2, A, 3, 9, 5, 10, 1, 1, 128, 128, 128, 128, 128, 1.0, 0),
+        "decode": lambda: _rc_decode(lib),
+        "gemm": lambda: L.la_gemm_bf16(A, A * 16, A * 64, 8, 8, 8, 8, 8, 8, 0),
+        "rmsnorm_rows": lambda: L.la_rmsnorm_rows(A, A * 2, A * 3, 4, 64, 64, 64, 1e-6, 0),
+        "gated_rmsnorm": lambda: L.la_gated_rmsnorm(A, A * 2, A * 3, A * 4, 4, 2, 128, 1e-6, 1, 0),
+    }
+
+
+def test_injected_launch_failure_is_reported_before_any_launch(lib, inject):
+    inject("launch")
+    for name, call in _valid_calls(lib).items():
+        assert call() == lib.LA_ERR_CUDA, name
+        assert "injected launch failure" in lib.last_error(), (name, lib.last_error())
+    # host checks still come first: a refused count is reported as such
+    assert _rc_conv(lib, 0, 10) == lib.LA_ERR_COUNT
+
+
+def test_injected_alloc_failure_is_reported(lib, inject):
+    inject("alloc")
+    calls = _valid_calls(lib)
+    for name in ("conv", "gdn_batched", "gdn_varlen_noalloc", "decode", "gemm"):
+        assert calls[name]() == lib.LA_ERR_CUDA, name
+        assert "injected allocation failure" in lib.last_error(), (name, lib.last_error())
+    assert lib._load().la_device_status(0) == -1  # the status word cannot be had either
+
+
+def test_unknown_injection_value_is_ignored(lib, inject):
+    inject("sometimes")
+    assert _rc_conv(lib, 0, 10) == lib.LA_ERR_COUNT
+    assert "injected" not in lib.last_error()
+
+
+def test_noalloc_binding_refuses_non_bf16(lib):
+    """The no-allocation call has no dtype argument (it is compiled for bf16): the binding
+    refuses any other dtype instead of letting the kernel read fp32 data as bf16."""
+    import torch
+    T, d = 4, 128
+    q = torch.zeros(T, d, dtype=torch.float32)
+    bf = torch.zeros(T, d, dtype=torch.bfloat16)
+    g = torch.zeros(T, 1)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    ptrs = torch.zeros(1, dtype=torch.int64)
+    for bad in ("q", "k", "v", "out"):
+        t = {n: bf for n in ("q", "k", "v")}
+        t["out"] = bf.view(T, 1, d)
+        t[bad] = q if bad != "out" else q.view(T, 1, d)
+        with pytest.raises(TypeError, match=bad):
+            lib.gdn_prefill_varlen_noalloc(ptrs, t["q"], t["k"], t["v"], g, g, t["out"], cu,
+                                           max_seqlen=T, Hk=1, Hv=1, dk=d, dv=d)

@@ -1,7 +1,10 @@
-"""Full-size workloads on the GPU, in the launch configuration the bench times (PrefillPass:
-conv1d+SiLU -> L2 -> recurrence through the C ABI), checked against the oracle on sampled
-(stream, v-head) units: every sampled unit's outputs, final state and the stream's conv state.
-Units are independent, so a sample is checked exactly as the whole would be.
+"""Full-size workloads on the GPU, through every public path the bench can report (PrefillPass:
+the one-launch la_prefill_front where it applies, the two-launch path — fused conv1d+SiLU+L2,
+then the recurrence — and, for a single stream, the segmented recurrence), checked against the
+oracle on sampled (stream, v-head) units: every sampled unit's outputs, final state and the
+stream's conv state. Units are independent, so a sample is checked exactly as the whole would
+be. The sample holds the shortest stream, whose units the longest-first scheduler hands out
+last (after every block has walked many units), the longest and the median one.
 """
 import math
 
@@ -9,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import linear_attention_chunked_conv1d_gb300 as la
 from linear_attention_chunked_conv1d_gb300.inputs import WORKLOADS, make_inputs
 from linear_attention_chunked_conv1d_gb300.path import PrefillPass
 from tests.helpers import TOL, f64, max_abs, oracle_front, oracle_recurrence, rel_frob
@@ -26,7 +30,20 @@ def sample_units(wl, lengths):
     return streams, heads
 
 
-def check_workload(wl, cuda, pad_fill=0.0, seed=0):
+def run_path(p, mode):
+    if mode == "run":
+        p.run()
+    elif mode == "split":
+        p.front_end()
+        p.recurrence()
+    elif mode == "seg":
+        p.front_end()
+        p.recurrence_segmented(2)
+    else:
+        raise ValueError(mode)
+
+
+def check_workload(wl, cuda, pad_fill=0.0, seed=0, mode="run"):
     inp = make_inputs(wl, device=cuda, seed=seed)
     lengths = inp["lengths"]
     cu = np.concatenate([[0], np.cumsum(lengths)])
@@ -36,8 +53,9 @@ def check_workload(wl, cuda, pad_fill=0.0, seed=0):
                     beta=inp["beta"][cu[s]:cu[s + 1]].cpu()) for s in streams}
     conv_w = inp["conv_w"].cpu()
     p = PrefillPass(wl, inp, pad_fill=pad_fill)
-    p.run()
+    run_path(p, mode)
     torch.cuda.synchronize()
+    assert la.device_status() == 0
     act = wl.dtype
     d = wl.d
     worst_o, worst_h = 0.0, 0.0
@@ -54,16 +72,27 @@ def check_workload(wl, cuda, pad_fill=0.0, seed=0):
         worst_o = max(worst_o, max_abs(got_o, ref_o))
         worst_h = max(worst_h, rel_frob(got_h, ref_h[0]))
     tol = TOL[act]
-    print(f"\n[parity] {wl.name}: max|o-o_ref| = {worst_o:.3e} (bar {tol['out']:.0e}), "
+    print(f"\n[parity] {wl.name} ({mode}): max|o-o_ref| = {worst_o:.3e} (bar {tol['out']:.0e}), "
           f"state rel.Frobenius = {worst_h:.3e} (bar {tol['state']:.0e})")
     assert worst_o <= tol["out"], f"{wl.name}: max |o - o_ref| = {worst_o:.3g}"
     assert worst_h <= tol["state"], f"{wl.name}: state rel. Frobenius error {worst_h:.3g}"
     return p
 
 
-@pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_full_size_sampled_parity(cuda, name):
-    check_workload(WORKLOADS[name], cuda)
+def _paths():
+    """(workload, path) pairs: every path PrefillPass offers for the workload."""
+    for name, wl in WORKLOADS.items():
+        tc = wl.dtype == "bf16" and wl.d == 128
+        yield name, "run"
+        if tc:  # run() is the one-launch path there; the two-launch path is a separate kernel
+            yield name, "split"
+        if tc and wl.B == 1:
+            yield name, "seg"
+
+
+@pytest.mark.parametrize("name,mode", list(_paths()))
+def test_workload_full_size_sampled_parity(cuda, name, mode):
+    check_workload(WORKLOADS[name], cuda, mode=mode)
     torch.cuda.empty_cache()
 
 

@@ -225,10 +225,21 @@ def test_conv_varlen_short_streams_carry_state():
     x = r.standard_normal((cu[-1], C))
     states = r.standard_normal((len(lengths), K - 1, C))
     w = r.standard_normal((C, K))
-    _, ns = oracle.conv1d_silu_varlen(states, x, w, cu)
+    out, ns = oracle.conv1d_silu_varlen(states, x, w, cu)
+    assert out.shape == x.shape
     for s, L in enumerate(lengths):
         xh = np.concatenate([states[s], x[cu[s]:cu[s + 1]]])
         np.testing.assert_array_equal(ns[s], xh[L:L + K - 1])
+        # each stream's rows of the packed output are that stream's own single-stream conv,
+        # which numpy.convolve over [its state ; its rows] gives independently
+        own, _ = oracle.conv1d_silu(states[s], x[cu[s]:cu[s + 1]], w)
+        np.testing.assert_array_equal(out[cu[s]:cu[s + 1]], own)
+        if L == 0:
+            continue
+        for c in range(C):
+            y = np.convolve(xh[:, c], w[c, ::-1], mode="valid")
+            np.testing.assert_allclose(out[cu[s]:cu[s + 1], c], y * expit(y), rtol=1e-13,
+                                       atol=1e-15)
 
 
 def test_l2norm_properties():
@@ -248,6 +259,96 @@ def test_l2norm_properties():
                                    rtol=1e-13, atol=1e-15)
     assert np.all(y[2, d:2 * d] == 0.0)
     np.testing.assert_array_equal(y[:, H * d:], x[:, H * d:])  # channels past the heads untouched
+
+
+# ---------------------------------------------------------------- the front end composition
+def _bf16(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _front_by_hand(x, w, states, cu, Hk, Hv, d, eps, *, swap_qk=False, round_conv=True,
+                   round_l2=True):
+    """The front end rebuilt from library routines only: numpy.convolve per channel over
+    [carried state ; the stream's rows] (reversed taps, valid mode), SiLU from scipy's logistic
+    function, bf16 rounding by torch, the L2 norm of each q and k head row by numpy.linalg, and
+    the [q heads | k heads | v heads] slices of the packed channels."""
+    T, C = x.shape
+    conv = np.zeros((T, C))
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        xh = np.concatenate([states[s], x[a:b]])
+        for c in range(C):
+            y = np.convolve(xh[:, c], w[c, ::-1], mode="valid")
+            conv[a:b, c] = y * expit(y)
+    if round_conv:
+        conv = _bf16(conv)
+    normed = conv.copy()
+    for h in range(2 * Hk):
+        blk = conv[:, h * d:(h + 1) * d]
+        normed[:, h * d:(h + 1) * d] = blk / np.sqrt(np.sum(blk * blk, axis=1, keepdims=True) + eps)
+    if round_l2:
+        normed = _bf16(normed)
+    q = normed[:, :Hk * d].reshape(T, Hk, d)
+    k = normed[:, Hk * d:2 * Hk * d].reshape(T, Hk, d)
+    v = normed[:, 2 * Hk * d:].reshape(T, Hv, d)
+    return (k, q, v) if swap_qk else (q, k, v)
+
+
+def test_front_end_composition_pinned():
+    """oracle.front_end (conv -> bf16 -> L2 of the q|k heads -> bf16 -> [q | k | v] slices, the
+    order of the conv_prefill, l2 and split launches of "glm5next_kda/prefill.rs") equals the
+    same steps rebuilt from numpy/scipy/torch routines, on two streams with carried states, and
+    the comparison is sensitive to a q/k swap and to a dropped rounding."""
+    r = rng(21)
+    Hk, Hv, d, K, eps = 1, 2, 4, 3, 1e-6
+    lengths = [5, 3]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    cd = 2 * Hk * d + Hv * d
+    x = _bf16(r.standard_normal((cu[-1], cd)))
+    w = _bf16(r.standard_normal((cd, K)) * 0.5)
+    states = _bf16(r.standard_normal((len(lengths), K - 1, cd)))
+    q, k, v, ns = oracle.front_end(x, w, states, cu, Hk=Hk, Hv=Hv, dk=d, dv=d, eps=eps,
+                                   act_dtype="bf16")
+    eq, ek, ev = _front_by_hand(x, w, states, cu, Hk, Hv, d, eps)
+    np.testing.assert_array_equal(q, eq)
+    np.testing.assert_array_equal(k, ek)
+    np.testing.assert_array_equal(v, ev)
+    for s, L in enumerate(lengths):
+        xh = np.concatenate([states[s], x[cu[s]:cu[s + 1]]])
+        np.testing.assert_array_equal(ns[s], xh[L:L + K - 1])
+    # q and k rows are unit vectors up to eps and bf16 rounding; v rows are not normalised
+    assert np.allclose(np.linalg.norm(q, axis=2), 1.0, atol=1e-2)
+    assert not np.allclose(np.linalg.norm(v, axis=2), 1.0, atol=1e-2)
+    # planted mistakes: each one changes the result
+    sq, sk, _ = _front_by_hand(x, w, states, cu, Hk, Hv, d, eps, swap_qk=True)
+    assert not np.array_equal(sq, q) and not np.array_equal(sk, k)
+    for kw in (dict(round_conv=False), dict(round_l2=False)):
+        mq, mk, mv = _front_by_hand(x, w, states, cu, Hk, Hv, d, eps, **kw)
+        assert not (np.array_equal(mq, q) and np.array_equal(mk, k) and np.array_equal(mv, v))
+
+
+def test_front_end_fp32_keeps_fp32_rounding():
+    """With fp32 activations the two stored steps round to fp32 (not bf16)."""
+    r = rng(22)
+    Hk, Hv, d, K, eps = 1, 1, 4, 4, 1e-6
+    cu = np.array([0, 6])
+    cd = 3 * d
+    x = r.standard_normal((6, cd)).astype(np.float32).astype(np.float64)
+    w = (r.standard_normal((cd, K)) * 0.5).astype(np.float32).astype(np.float64)
+    st = np.zeros((1, K - 1, cd))
+    q, k, v, _ = oracle.front_end(x, w, st, cu, Hk=Hk, Hv=Hv, dk=d, dv=d, eps=eps,
+                                  act_dtype="f32")
+    conv = np.zeros((6, cd))
+    xh = np.concatenate([st[0], x])
+    for c in range(cd):
+        y = np.convolve(xh[:, c], w[c, ::-1], mode="valid")
+        conv[:, c] = y * expit(y)
+    conv = conv.astype(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(v.reshape(6, d), conv[:, 2 * d:])
+    blk = conv[:, d:2 * d]
+    ek = (blk / np.sqrt(np.sum(blk * blk, axis=1, keepdims=True) + eps)).astype(np.float32)
+    np.testing.assert_array_equal(k.reshape(6, d), ek.astype(np.float64))
 
 
 # ---------------------------------------------------------------- invariants

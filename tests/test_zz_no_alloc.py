@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import linear_attention_chunked_conv1d_gb300 as la
+import oracle
 from linear_attention_chunked_conv1d_gb300.inputs import recurrence_inputs
 from tests.helpers import TOL, f64, max_abs, rel_frob
 
@@ -41,15 +42,43 @@ def _run(cuda, inp, noalloc):
     return out.cpu(), h.cpu()
 
 
+def _oracle(inp):
+    lengths = inp["lengths"]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    d = inp["q"].shape[2]
+    return oracle.gated_delta(f64(inp["h"]), f64(inp["q"]), f64(inp["k"]), f64(inp["v"]),
+                              f64(inp["g"]), f64(inp["beta"]), cu, scale=1.0 / math.sqrt(d))
+
+
 def test_noalloc_matches_workspace_call_twice_in_a_row(cuda):
-    tol = TOL["bf16"]
-    cases = [recurrence_inputs([130, 1, 64, 0, 257], 2, 4, 128, seed=501),
+    """Same kernel, same inputs: the no-allocation call gives the bits of the workspace call.
+    The calls run back to back on the shared scratch; the first case has 200 streams, whose
+    stream order fills the bytes where the later, smaller calls keep their unit counter, so
+    those calls only work if each call re-initialises what it reads."""
+    r = np.random.default_rng(500)
+    many = [int(v) for v in r.integers(0, 40, size=200)]
+    cases = [recurrence_inputs(many, 1, 2, 128, seed=500),
+             recurrence_inputs([130, 1, 64, 0, 257], 2, 4, 128, seed=501),
              recurrence_inputs([70, 300], 1, 2, 128, seed=502)]
-    for inp in cases:  # two calls in a row reuse (and must re-initialise) the shared scratch
+    for i, inp in enumerate(cases):
         o_ref, h_ref = _run(cuda, inp, noalloc=False)
         o_na, h_na = _run(cuda, inp, noalloc=True)
-        assert max_abs(f64(o_na), f64(o_ref)) <= tol["out"]
-        assert rel_frob(f64(h_na), f64(h_ref)) <= tol["state"]
+        assert torch.equal(o_na, o_ref), i
+        assert torch.equal(h_na, h_ref), i
+        if i == 1:  # and once against the oracle directly
+            ref_o, ref_h = _oracle(inp)
+            tol = TOL["bf16"]
+            assert max_abs(f64(o_na), ref_o) <= tol["out"]
+            assert rel_frob(f64(h_na), ref_h) <= tol["state"]
+
+
+def test_noalloc_accepts_the_stream_limit(cuda):
+    """4096 one-token streams, the most the fixed scratch serves, then a 3-stream call."""
+    for lengths in ([1] * 4096, [5, 9, 2]):
+        inp = recurrence_inputs(lengths, 1, 1, 128, seed=503)
+        o_ref, h_ref = _run(cuda, inp, noalloc=False)
+        o_na, h_na = _run(cuda, inp, noalloc=True)
+        assert torch.equal(o_na, o_ref) and torch.equal(h_na, h_ref)
 
 
 def test_noalloc_refuses_too_many_streams(cuda):
