@@ -11,8 +11,8 @@
 // Per chunk of C = 64 tokens (t, i: tokens; c: k-channel; d: v-channel; S = H^T [d][c], fp32,
 // resident in TMEM for the whole unit; gc: inclusive cumulative log-gate, pad rows g = 0):
 //   D1 = [K ; Q] K^T                     tensor core (GDN: bf16 inputs as loaded;
-//                                        KDA: tf32, with decays split at the mid row m:
-//                                        [K e^{gc-gc_m} ; Q e^{gc-gc_m}] (K e^{gc_m-gc})^T)
+//                                        KDA: tf32, with the decays split per factor:
+//                                        [K e^gc ; Q e^gc] (K e^{-gc})^T)
 //   A  = strictly-lower(beta_t e^{gc_t-gc_i} D1_KK),  P = lower(e^{gc_t-gc_i} D1_QK)
 //   T  = (I + A)^{-1}                    CUDA cores, forward substitution per column
 //   D2 = S [K e^gc ; Q e^gc]^T           tensor core (tf32, A operand read from TMEM)
@@ -22,9 +22,10 @@
 //   S  <- S diag(e^{gc_L}) + U'^T (K e^{gc_L - gc})     tensor core, accumulating into S
 //   o  = scale O                          epilogue
 // which is the token recurrence S_t = S_{t-1} diag(a_t)(I - b_t k_t k_t^T) + b_t v_t k_t^T,
-// o_t = scale S_t q_t, unrolled over the chunk. Every exponent is <= 0 except the KDA
-// mid-row split, whose range is checked per chunk; a chunk whose half-chunk decay exceeds
-// e^80 in some channel takes an exact pairwise-exponent path for D1 on the CUDA cores.
+// o_t = scale S_t q_t, unrolled over the chunk. Every exponent is <= 0 except the two split
+// decays of D1 (GDN: at the mid row, KDA: e^{-gc}), whose range is checked per chunk; a chunk
+// whose decay exceeds e^80 (GDN: in either half, KDA: in some channel over the whole chunk)
+// takes an exact pairwise-exponent path for D1 on the CUDA cores.
 //
 // Fused front end (FRONT): the block also computes its q, k and v tiles, chunk by chunk, from
 // the pre-conv rows x — causal depthwise conv over the carried conv state, SiLU, and the L2
@@ -43,6 +44,7 @@
 // accumulation is fp32. Rows at or past a stream's end are removed by selects.
 #include <mutex>
 
+#include "chunk_tiles.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "tc.cuh"
@@ -50,6 +52,8 @@
 namespace la {
 
 namespace {
+
+using namespace tiles;
 
 constexpr int TC_C = 64;         // chunk
 constexpr int TC_D = 128;        // dk = dv
@@ -104,42 +108,6 @@ struct TcParams {
     int *conv_readers;    // fused front end: [B][Hk] readers of the old conv state so far
     int num_units;
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Wait until at most the most recent committed group of this thread is still in flight.
-__device__ __forceinline__ void cp_async_wait_but_last() {
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// Byte offsets of one column (element k) of a K-major SW128 tile with R rows: row t sits at
-// off[t % 8] + (t / 8) * 1024, so fully unrolled walks down a column need no address math.
-struct ColWalk {
-    uint32_t off[8];
-    __device__ __forceinline__ void init(uint32_t base, uint32_t k, uint32_t R, uint32_t es) {
-#pragma unroll
-        for (uint32_t r = 0; r < 8; ++r) off[r] = base + tc::sw128_offset(r, k, R, es);
-    }
-    __device__ __forceinline__ uint32_t at(int t) const {
-        return off[t & 7] + static_cast<uint32_t>(t >> 3) * 1024u;
-    }
-};
-
-__device__ __forceinline__ float ld_bf16(const unsigned char *sm, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off));
-}
-__device__ __forceinline__ void st_tf32(unsigned char *sm, uint32_t off, float v) {
-    *reinterpret_cast<float *>(sm + off) = tc::to_tf32(v);
-}
 
 // Issue the K, Q (k-head kh) and V (v-head j) rows of one chunk as 16-byte async copies into
 // the swizzled tiles; rows >= n are zero-filled (their source is never read).
@@ -602,7 +570,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     sf[SF_GL + row] = gcr[C16 - 1];
                     sf[SF_EL + row] = __expf(gcr[C16 - 1]);
                 }
-                if (part == NQ / 2 - 1) sf[SF_GM + row] = gcr[C16 - 1];
             } else if (tid < TC_C) {
                 const float gct = sf[SF_GC + tid] + (tid >= 32 ? sf[SF_WARP] : 0.f);
                 sf[SF_GC + tid] = gct;
@@ -633,24 +600,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 sf[SF_CF + tid] = __expf(gm - gct);
             }
 
-            // ---------------- D1 = [K;Q] K^T (KDA: decays split at row 31); GDN also K^T
+            // ---------------- D1 = [K;Q] K^T (KDA: tf32, decays split per factor); GDN also K^T
             bool slow = false;
-            if (KDA) wait_state();  // the Kr tile below is the previous state update's operand
+            if (KDA) wait_state();  // the Kinv tile below is the previous state update's operand
             if (KDA) {
+                // [K e^gc ; Q e^gc] (D1's A operand, then the state MMA's) and Kinv = K e^{-gc}
+                // (D1's B operand), rows >= n zero: D1 = [K;Q] K^T with e^{gc_t - gc_i} split as
+                // e^{gc_t} e^{-gc_i}, valid while the chunk's decay e^{-gc_L} stays below e^80
                 const int c = row;
-                const float gm = sf[SF_GM + c];
                 const float gLc = sf[SF_GL + c];
-                if (part == NQ / 2 - 1 && -gm > 80.f) *slow_sh = 1;
-                if (part == NQ - 1 && gm - gLc > 80.f) *slow_sh = 1;
+                if (part == NQ - 1 && -gLc > 80.f) *slow_sh = 1;
 #pragma unroll
                 for (int t = 0; t < C16; ++t) {
                     const int tt = C16 * part + t;
+                    const bool valid = tt < n;
                     const float kv = ld_bf16(sm, w_kq.at(tt));
                     const float qv = ld_bf16(sm, w_kq.at(64 + tt));
-                    const float f1 = __expf(gcr[t] - gm), f2 = __expf(gm - gcr[t]);
-                    st_tf32(sm, w_kqg.at(tt), kv * f1);
-                    st_tf32(sm, w_kqg.at(64 + tt), qv * f1);
-                    st_tf32(sm, w_kr.at(tt), kv * f2);
+                    const float eg = __expf(gcr[t]), ei = __expf(-gcr[t]);
+                    st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
+                    st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
+                    st_tf32(sm, w_kr.at(tt), valid ? kv * ei : 0.f);
                 }
                 tc::fence_async_smem();
                 __syncthreads();
@@ -775,7 +744,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             if (!slow) {
                 wait_bar(bar_a, phase_a);
             } else if (KDA) {
-                float *gct = reinterpret_cast<float *>(sm + SM_KQG);  // [64][128] fp32
+                float *gct = reinterpret_cast<float *>(sm + SM_KDT);  // [64][128] fp32
 #pragma unroll
                 for (int t = 0; t < C16; ++t) gct[(C16 * part + t) * TC_D + row] = gcr[t];
                 __syncthreads();
@@ -865,8 +834,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             tc::fence_before_sync();
             __syncthreads();
 
-            if (KDA) {  // KDA: the Kl|Ql and Kr buffers are free now
-                // [K e^gc ; Q e^gc] and (K e^{gc_L - gc})^T, thread per (channel, row part)
+            if (KDA) {  // KDA: D1 is complete, its B operand's buffer (or the exact path's gate
+                        // table) is free: (K e^{gc_L - gc})^T, thread per (channel, row part)
                 const int c = row;
                 const float gLc = sf[SF_GL + c];
                 float kd[4];
@@ -875,10 +844,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                     const int tt = C16 * part + t;
                     const bool valid = tt < n;
                     const float kv = ld_bf16(sm, w_kq.at(tt));
-                    const float qv = ld_bf16(sm, w_kq.at(64 + tt));
-                    const float eg = __expf(gcr[t]), egl = __expf(gLc - gcr[t]);  // both <= 1
-                    st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
-                    st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
+                    const float egl = __expf(gLc - gcr[t]);  // <= 1
                     kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
                     if ((t & 3) == 3) {
                         *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =

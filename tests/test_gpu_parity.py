@@ -360,3 +360,17 @@ def test_gdn_extreme_gates_exact_decay_path(cuda):
     o, h = run_rec(cuda, inp, 2, 4, 128, kda=False, mode="varlen")
     assert torch.isfinite(o.float()).all() and torch.isfinite(h).all()
     check_parity(inp, o, h, 2, 4, 128, False, "bf16")
+
+
+def test_kda_decay_near_split_limit(cuda):
+    """KDA's D1 splits each decay as e^{gc_t} e^{-gc_i}; the fast path holds while a chunk's
+    decay stays below e^80 in every channel. Channels decaying by e^-78 per chunk (just inside)
+    and by e^-83 (just past, exact path) must both match the oracle."""
+    inp = recurrence_inputs([64 * 4, 100], 1, 2, 128, kda=True, dtype="bf16", seed=95)
+    g = inp["g"].clone()
+    g[:, 0, :16] = -78.0 / 64    # fast path at its edge: e^{-gc} up to e^78
+    g[:, 1, 16:24] = -83.0 / 64  # the exact pairwise path
+    inp["g"] = g
+    o, h = run_rec(cuda, inp, 1, 2, 128, kda=True, mode="varlen")
+    assert torch.isfinite(o.float()).all() and torch.isfinite(h).all()
+    check_parity(inp, o, h, 1, 2, 128, True, "bf16")
