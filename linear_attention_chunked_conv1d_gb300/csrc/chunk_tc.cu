@@ -42,6 +42,8 @@
 // the two intermediate products of the block substitution (U'0 and Z, inside U' = R T^T),
 // which the next MMA reads from TMEM without that rounding step;
 // accumulation is fp32. Rows at or past a stream's end are removed by selects.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "chunk_tiles.cuh"
@@ -88,10 +90,10 @@ constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 
                    SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704 /* [NQ][128] */,
                    SF_WARP = 704 + 128 * NQ, SF_RF = SF_WARP + 8, SF_CF = SF_RF + 64,
                    SF_END = SF_CF + 64;
-constexpr uint32_t SM_BARS = SM_SMALL + SF_END * 4;  // mbarriers, flags, tmem base (64 B)
+constexpr uint32_t SM_BARS = SM_SMALL + SF_END * 4;  // mbarriers, flags, tmem base (128 B)
 // fused front end: conv taps (fp32 [4 taps][3 x 128 channels], leading taps zero when
 // kernel < 4) and bias of the unit's q | k | v channels; the raw rows share the tf32 K|Q buffer
-constexpr uint32_t SM_CW = SM_BARS + 64;
+constexpr uint32_t SM_CW = SM_BARS + 128;
 constexpr uint32_t SM_CB = SM_CW + 3 * TC_D * 16;
 constexpr uint32_t SM_RAW = SM_KQG;             // bf16 [67 rows][384 channels]
 constexpr int RAW_ROWS = TC_C + 3;              // chunk + halo of the longest conv (4 taps)
@@ -107,6 +109,11 @@ struct TcParams {
     int *counter;         // unit claim counter (zeroed by the order kernel)
     int *conv_readers;    // fused front end: [B][Hk] readers of the old conv state so far
     int num_units;
+    // Plain recurrence calls: the K, Q and V tiles arrive by TMA, boxes of 64 rows x 64
+    // channels of [tokens][heads x 128] (rows past the last token read as zero); otherwise
+    // (fused front end, segmented scan) by 16-byte async copies.
+    int tma;
+    CUtensorMap map_k, map_q, map_v;
 };
 
 // Issue the K, Q (k-head kh) and V (v-head j) rows of one chunk as 16-byte async copies into
@@ -321,7 +328,7 @@ __device__ __forceinline__ bool sync_ok(volatile int *flag) {
 }
 
 template <bool KDA, bool FRONT>
-__global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams P) {
+__global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_constant__ TcParams P) {
     const RecArgs &a = P.a;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm =
@@ -334,6 +341,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     uint64_t *bar_c = reinterpret_cast<uint64_t *>(sm + SM_BARS + 40);  // state update done
     uint64_t *bar_d = reinterpret_cast<uint64_t *>(sm + SM_BARS + 48);  // block-substitution steps
     uint64_t *bar_e = reinterpret_cast<uint64_t *>(sm + SM_BARS + 56);  // final drain of the MMAs
+    uint64_t *bar_kq = reinterpret_cast<uint64_t *>(sm + SM_BARS + 64);  // K|Q tile by TMA
+    uint64_t *bar_v = reinterpret_cast<uint64_t *>(sm + SM_BARS + 72);   // V tile by TMA
     volatile int *err = reinterpret_cast<volatile int *>(sm + SM_BARS + 16);
     volatile int *unit_sh = err + 1;
     volatile int *slow_sh = err + 2;
@@ -356,6 +365,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         tc::mbar_init(bar_c, 1);
         tc::mbar_init(bar_d, 1);
         tc::mbar_init(bar_e, 1);
+        tc::mbar_init(bar_kq, 1);
+        tc::mbar_init(bar_v, 1);
         tc::fence_mbar_init();
     }
     // identity tile (bf16, K-major 64x64) for the transposing MMAs
@@ -394,6 +405,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         }
     };
 
+    // TMA loads of the K|Q and V tiles (plain calls): thread 0 issues the boxes of a chunk, one
+    // load per tile and chunk in flight at most; every thread waits for a tile's phase before
+    // its first use (par_*: parity of the next load to be consumed; fly_*: thread 0's record of
+    // an issued load that has not been consumed, drained on exit)
+    const bool use_tma = !FRONT && P.tma != 0;
+    uint32_t par_kq = 0, par_v = 0;
+    bool fly_kq = false, fly_v = false;
+    auto tma_kq = [&](int kh_, int tok) {
+        if (tid == 0) {
+            tc::fence_async_smem();  // earlier generic accesses of the tile come first
+            tc::mbar_expect_tx(bar_kq, 32768u);
+            const int x = kh_ * TC_D;
+            tc::tma_load_2d(sb + SM_KQ, &P.map_k, x, tok, bar_kq);           // K, channels 0-63
+            tc::tma_load_2d(sb + SM_KQ + 16384, &P.map_k, x + 64, tok, bar_kq);  // K, 64-127
+            tc::tma_load_2d(sb + SM_KQ + 8192, &P.map_q, x, tok, bar_kq);    // Q rows 64.. of the tile
+            tc::tma_load_2d(sb + SM_KQ + 24576, &P.map_q, x + 64, tok, bar_kq);
+            fly_kq = true;
+        }
+    };
+    auto tma_v = [&](int j_, int tok) {
+        if (tid == 0) {
+            tc::fence_async_smem();
+            tc::mbar_expect_tx(bar_v, 16384u);
+            const int x = j_ * TC_D;
+            tc::tma_load_2d(sb + SM_V, &P.map_v, x, tok, bar_v);
+            tc::tma_load_2d(sb + SM_V + 8192, &P.map_v, x + 64, tok, bar_v);
+            fly_v = true;
+        }
+    };
+    auto tma_wait = [&](uint64_t *bar, uint32_t par) {
+        if (!tc::mbar_wait(bar, par, wait_ns)) *err = 1;
+    };
+
     ColWalk w_kq, w_kqg, w_kr;
     w_kq.init(SM_KQ, row, 128, 2);    // column c of the bf16 K|Q tile
     w_kqg.init(SM_KQG, row, 128, 4);  // column c of the tf32 K|Q tile
@@ -429,6 +473,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
         if (FRONT) {
             load_conv_weights(a, sm, kh, j, tid);
             load_raw(a, sm, conv_state, t0, len, 0, kh, j, tid);
+        } else if (use_tma && !alt) {
+            tma_kq(kh, t0);
+            tma_v(j, t0);
         } else {
             load_kq(a, sm, t0, min(TC_C, len), kh, tid);
             load_v(a, sm, t0, min(TC_C, len), j, tid, alt);
@@ -551,6 +598,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 }
             }
             cp_async_wait_all();
+            if (use_tma) {  // this chunk's K|Q and V tiles (the K|Q may have been waited already)
+                tma_wait(bar_kq, par_kq);
+                tma_wait(bar_v, par_v);
+                par_kq ^= 1u;
+                par_v ^= 1u;
+                if (tid == 0) fly_kq = fly_v = false;
+            }
             tc::fence_async_smem();
             if (a.debug_stall) {  // test knob: a wait on a barrier nothing completes runs out
                 uint32_t never = 0;
@@ -576,15 +630,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
                 sf[SF_GC2 + tid] = gct * LOG2E;
             }
             // Pad rows of the K|Q tile carry pad_fill; every consumer removes them by select.
-            // (The V tile keeps the zeros of the async copy: it is contracted over tokens by
-            // the transposing MMA, where a NaN row would reach every column even through an
-            // exact zero weight.)
-            if (!FRONT && n < TC_C && a.pad_fill != 0.f) {
+            // The V tile's pad rows are zero: it is contracted over tokens by the transposing
+            // MMA, where a NaN row would reach every column even through an exact zero weight.
+            // (Async copies zero-fill those rows; a TMA box brings the next stream's rows,
+            // rewritten here before any use.)
+            if (!FRONT && n < TC_C && (use_tma || a.pad_fill != 0.f)) {
                 const __nv_bfloat16 pf = __float2bfloat16_rn(a.pad_fill);
                 for (int idx = tid; idx < (TC_C - n) * TC_D; idx += TC_THREADS) {
                     const int r = n + idx / TC_D, c = idx % TC_D;
                     *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(r, c, 128, 2)) = pf;
                     *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(64 + r, c, 128, 2)) = pf;
+                    if (use_tma && !alt)
+                        *reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + tc::sw128_offset(r, c, 64, 2)) =
+                            __float2bfloat16_rn(0.f);
                 }
                 tc::fence_async_smem();
             }
@@ -775,7 +833,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             }
             if (!sync_ok(err)) break;
             if (!KDA && !FRONT && !last) {  // GDN: K|Q tile consumed (D1, K^T, staging)
-                load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+                if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
+                else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
             }
 
@@ -909,7 +968,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             __syncthreads();
             if (!last) {  // KDA: K|Q tile consumed by the staging: next chunk's K, Q and gates
                 if (KDA && !FRONT) {
-                    load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+                    if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
+                    else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                     cp_async_commit();
                 }
                 if (KDA) {
@@ -929,6 +989,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             if (!last) {  // V tile consumed by the identity MMA: next chunk's V (FRONT: the
                           // raw rows, into the tf32 K|Q buffer the state MMA has read) in flight
                 if (FRONT) load_raw(a, sm, nullptr, t0, len, (ch + 1) * TC_C, kh, j, tid);
+                else if (use_tma && !alt) tma_v(j, tok0 + TC_C);
                 else load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid, alt);
                 cp_async_commit();
             }
@@ -952,7 +1013,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
             // the V copies just issued may stay in flight) have landed for every thread after
             // the barrier below, and its tf32 copy can be staged during the chain
             const bool stage_ahead = !KDA && !FRONT && !last;
-            if (stage_ahead) cp_async_wait_but_last();
+            if (stage_ahead) {
+                if (use_tma && !alt) tma_wait(bar_kq, par_kq);  // the next chunk's K|Q
+                else cp_async_wait_but_last();
+            }
             tc::fence_before_sync();
             __syncthreads();
 
@@ -1119,6 +1183,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const TcParams 
     }
 
     cp_async_wait_all();
+    // a TMA load still in flight after an error lands before the block exits
+    if (tid == 0 && fly_kq) tc::mbar_wait(bar_kq, par_kq, WAIT_NS);
+    if (tid == 0 && fly_v) tc::mbar_wait(bar_v, par_v, WAIT_NS);
     // Every MMA of this block has completed before its TMEM is released, also after a wait gave
     // up: the issuing lane commits once more (a commit tracks all earlier MMAs of its thread)
     // and waits for that commit with the full limit.
@@ -1231,6 +1298,13 @@ cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st) {
     P.counter = counter;
     P.conv_readers = readers;
     P.num_units = a.B * a.Hv;
+    // K, Q, V by TMA for the plain calls (2-D maps over [tokens][heads x 128], 64 x 64 boxes,
+    // 128-byte swizzle); the async-copy path stays for the fused front end and the segmented
+    // scan, and in case a map cannot be encoded
+    P.tma = !a.front && !a.use_alt &&
+            make_map_bf16_2d(&P.map_k, a.k, a.total, (int64_t)a.Hk * TC_D, a.k_stride, 64, 64, true) &&
+            make_map_bf16_2d(&P.map_q, a.q, a.total, (int64_t)a.Hk * TC_D, a.q_stride, 64, 64, true) &&
+            make_map_bf16_2d(&P.map_v, a.v, a.total, (int64_t)a.Hv * TC_D, a.v_stride, 64, 64, true);
     const int grid = min(P.num_units, sm_count());
     auto kern = a.kda ? (a.front ? chunk_tc_kernel<true, true> : chunk_tc_kernel<true, false>)
                       : (a.front ? chunk_tc_kernel<false, true> : chunk_tc_kernel<false, false>);

@@ -38,22 +38,8 @@ constexpr int G_THREADS = 192;
 constexpr uint32_t ACC_COLS = 2 * GN;             // two accumulators
 constexpr uint64_t G_WAIT_NS = 2000000000ull;
 
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
-// 2-D tiled TMA load of the box at (x = inner coordinate, y) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
-        : "memory");
 }
 
 __global__ void __launch_bounds__(G_THREADS, 1)
@@ -109,9 +95,9 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                         *err = 1;
                         break;
                     }
-                    mbar_expect_tx(full + s, STAGE_BYTES);
-                    tma_load_2d(sbase + s * STAGE_BYTES, &map_a, k * GK, m0, full + s);
-                    tma_load_2d(sbase + s * STAGE_BYTES + A_BYTES, &map_w, k * GK, n0, full + s);
+                    tc::mbar_expect_tx(full + s, STAGE_BYTES);
+                    tc::tma_load_2d(sbase + s * STAGE_BYTES, &map_a, k * GK, m0, full + s);
+                    tc::tma_load_2d(sbase + s * STAGE_BYTES + A_BYTES, &map_w, k * GK, n0, full + s);
                 }
             }
             // every copy this thread issued must have landed before the block exits: the last

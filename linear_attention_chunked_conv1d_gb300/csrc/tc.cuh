@@ -226,6 +226,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// Arrival that also expects `bytes` of asynchronous copies (TMA) to complete on this phase.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// 2-D tiled TMA load of the box at (x = inner coordinate, y) into shared memory, completing
+// `bar`'s transaction count. `map` is a CUtensorMap in parameter, constant or global memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 2^x on the special-function unit (ex2.approx.ftz: relative error below 2^-22; x <= 0 in
 // every use here, so no overflow path is needed).
 __device__ __forceinline__ float ex2(float x) {
