@@ -374,3 +374,22 @@ def test_kda_decay_near_split_limit(cuda):
     o, h = run_rec(cuda, inp, 1, 2, 128, kda=True, mode="varlen")
     assert torch.isfinite(o.float()).all() and torch.isfinite(h).all()
     check_parity(inp, o, h, 1, 2, 128, True, "bf16")
+
+
+@pytest.mark.parametrize("kda", [False, True])
+def test_next_stream_rows_do_not_reach_a_stream(cuda, kda):
+    """The tensor-core path loads 64-row boxes, so a stream's last chunk also brings rows of the
+    next stream; they are rewritten (pad value, zero V) before any use. A stream's outputs and
+    state must keep their bits whatever the next stream holds, NaN included."""
+    lengths = [70, 50]
+    inp = recurrence_inputs(lengths, 1, 2, 128, kda=kda, dtype="bf16", seed=97)
+    o_a, h_a = run_rec(cuda, inp, 1, 2, 128, kda=kda, mode="varlen")
+    poisoned = dict(inp)
+    for name in ("q", "k", "v"):
+        t = inp[name].clone()
+        t[lengths[0]:] = float("nan")
+        poisoned[name] = t
+    o_b, h_b = run_rec(cuda, poisoned, 1, 2, 128, kda=kda, mode="varlen")
+    assert torch.equal(o_a[:lengths[0]], o_b[:lengths[0]])
+    assert torch.equal(h_a[0], h_b[0])
+    check_parity(inp, o_a, h_a, 1, 2, 128, kda, "bf16")
