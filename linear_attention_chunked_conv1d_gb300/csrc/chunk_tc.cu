@@ -1204,20 +1204,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 }
 
 // Orders the streams by decreasing length (stable) so that the longest units start first,
-// and zeroes the unit counter. One block; B <= 1024 per pass of the rank computation.
+// and zeroes the unit counter. One block: each thread ranks its streams against all B lengths,
+// read from shared memory (staged there first) when B fits, else from cu_seqlens. Equal
+// lengths (the batched call) keep their order.
+constexpr int kOrderStaged = 8192;
 __global__ void order_streams_kernel(const int32_t *cu, int B, int T_each, int32_t *perm,
                                      int *counter, int *conv_readers, int n_readers) {
+    __shared__ int lens[kOrderStaged];
     for (int i = threadIdx.x; i < n_readers; i += blockDim.x) conv_readers[i] = 0;
+    if (threadIdx.x == 0) *counter = 0;
+    if (!cu) {
+        for (int s = threadIdx.x; s < B; s += blockDim.x) perm[s] = s;
+        return;
+    }
+    const bool staged = B <= kOrderStaged;
+    if (staged)
+        for (int s = threadIdx.x; s < B; s += blockDim.x) lens[s] = cu[s + 1] - cu[s];
+    __syncthreads();
     for (int s = threadIdx.x; s < B; s += blockDim.x) {
-        const int ls = cu ? cu[s + 1] - cu[s] : T_each;
+        const int ls = staged ? lens[s] : cu[s + 1] - cu[s];
         int rank = 0;
         for (int o = 0; o < B; ++o) {
-            const int lo = cu ? cu[o + 1] - cu[o] : T_each;
+            const int lo = staged ? lens[o] : cu[o + 1] - cu[o];
             rank += (lo > ls) || (lo == ls && o < s);
         }
         perm[rank] = s;
     }
-    if (threadIdx.x == 0) *counter = 0;
 }
 
 int sm_count() {
