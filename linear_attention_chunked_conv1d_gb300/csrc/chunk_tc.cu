@@ -1204,32 +1204,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 }
 
 // Orders the streams by decreasing length (stable) so that the longest units start first,
-// and zeroes the unit counter. One block: each thread ranks its streams against all B lengths,
-// read from shared memory (staged there first) when B fits, else from cu_seqlens. Equal
-// lengths (the batched call) keep their order.
+// and zeroes the unit counter (and the conv-state reader counts). One thread per stream ranks
+// it against all B lengths, read from shared memory (each block stages them first) when B fits,
+// else from cu_seqlens; blocks of ORDER_THREADS streams run side by side. Equal lengths (the
+// batched call) keep their order.
 constexpr int kOrderStaged = 8192;
-__global__ void order_streams_kernel(const int32_t *cu, int B, int T_each, int32_t *perm,
-                                     int *counter, int *conv_readers, int n_readers) {
+constexpr int ORDER_THREADS = 256;
+__global__ void __launch_bounds__(ORDER_THREADS)
+order_streams_kernel(const int32_t *cu, int B, int T_each, int32_t *perm, int *counter,
+                     int *conv_readers, int n_readers) {
     __shared__ int lens[kOrderStaged];
-    for (int i = threadIdx.x; i < n_readers; i += blockDim.x) conv_readers[i] = 0;
-    if (threadIdx.x == 0) *counter = 0;
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < n_readers; i += blockDim.x) conv_readers[i] = 0;
+        if (threadIdx.x == 0) *counter = 0;
+    }
+    const int s = blockIdx.x * ORDER_THREADS + threadIdx.x;
     if (!cu) {
-        for (int s = threadIdx.x; s < B; s += blockDim.x) perm[s] = s;
+        if (s < B) perm[s] = s;
         return;
     }
     const bool staged = B <= kOrderStaged;
     if (staged)
-        for (int s = threadIdx.x; s < B; s += blockDim.x) lens[s] = cu[s + 1] - cu[s];
+        for (int o = threadIdx.x; o < B; o += blockDim.x) lens[o] = cu[o + 1] - cu[o];
     __syncthreads();
-    for (int s = threadIdx.x; s < B; s += blockDim.x) {
-        const int ls = staged ? lens[s] : cu[s + 1] - cu[s];
-        int rank = 0;
-        for (int o = 0; o < B; ++o) {
-            const int lo = staged ? lens[o] : cu[o + 1] - cu[o];
-            rank += (lo > ls) || (lo == ls && o < s);
-        }
-        perm[rank] = s;
+    if (s >= B) return;
+    const int ls = staged ? lens[s] : cu[s + 1] - cu[s];
+    int rank = 0;
+    for (int o = 0; o < B; ++o) {
+        const int lo = staged ? lens[o] : cu[o + 1] - cu[o];
+        rank += (lo > ls) || (lo == ls && o < s);
     }
+    perm[rank] = s;
 }
 
 int sm_count() {
@@ -1300,8 +1305,8 @@ cudaError_t launch_chunk_tc(const RecArgs &a, cudaStream_t st) {
     int32_t *perm = reinterpret_cast<int32_t *>(ws);
     int *readers = a.front ? reinterpret_cast<int *>(ws + order_bytes(a.B)) : nullptr;
     int *counter = reinterpret_cast<int *>(ws + chunk_tc_workspace_bytes(a.B, a.front ? a.Hk : 0) - 256);
-    order_streams_kernel<<<1, 1024, 0, st>>>(a.cu, a.B, a.T_each, perm, counter, readers,
-                                             a.front ? a.B * a.Hk : 0);
+    order_streams_kernel<<<(a.B + ORDER_THREADS - 1) / ORDER_THREADS, ORDER_THREADS, 0, st>>>(
+        a.cu, a.B, a.T_each, perm, counter, readers, a.front ? a.B * a.Hk : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     TcParams P;
