@@ -74,8 +74,8 @@ extern "C" {
 /* Every wait of the tensor-core kernels on an mbarrier (MMA or copy completion) gives up after
  * 2 s; the block then drains its own MMAs and copies, frees its tensor memory, raises
  * LA_DEV_TIMEOUT and exits, so the context stays usable. Two environment variables, read at
- * every call, exist to test that path: LA_WAIT_LIMIT_NS (a positive integer) replaces the 2 s
- * limit, and LA_DEBUG_STALL=1 makes each block of those kernels wait once on a barrier that
+ * every call, exist to test that path: LA_WAIT_LIMIT_NS (a positive integer, raised to at least
+ * 1 ms) replaces the 2 s limit, and LA_DEBUG_STALL=1 makes each block of those kernels wait once on a barrier that
  * nothing completes, so that the wait runs out. Neither is meant for production use. */
 
 /* ABI version of this header (bumped on any signature change). */

@@ -78,13 +78,15 @@ int get_status(int **out) {
 }
 
 // Limit of the bounded waits inside the tensor-core kernels: 2 s, or LA_WAIT_LIMIT_NS (a test
-// knob that lets a wait run out on purpose; read at every call).
+// knob that lets a wait run out on purpose; read at every call), never below 1 ms: the kernels'
+// block-wide error checks rely on a wait running at least that long before it gives up.
 uint64_t wait_limit_ns() {
+    constexpr uint64_t kMin = 1000000ull;
     const char *v = getenv("LA_WAIT_LIMIT_NS");
     if (v && *v) {
         char *end = nullptr;
         const unsigned long long n = strtoull(v, &end, 10);
-        if (end && *end == '\0' && n > 0) return (uint64_t)n;
+        if (end && *end == '\0' && n > 0) return n < kMin ? kMin : (uint64_t)n;
     }
     return 2000000000ull;
 }
