@@ -441,7 +441,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
     ColWalk w_kq, w_kqg, w_kr;
     w_kq.init(SM_KQ, row, 128, 2);    // column c of the bf16 K|Q tile
     w_kqg.init(SM_KQG, row, 128, 4);  // column c of the tf32 K|Q tile
-    w_kr.init(SM_KDT, row, 64, 4);    // column c of the tf32 Kr tile (KDA)
+    w_kr.init(SM_P, row, 64, 4);      // column c of the tf32 Kinv tile (KDA; D1's B operand
+                                      // in the P | T00 | T11 | -A10 space, free until D1)
 
     const float scale = a.scale;
     const int Hv = a.Hv, group = a.Hv / a.Hk;
@@ -660,14 +661,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 
             // ---------------- D1 = [K;Q] K^T (KDA: tf32, decays split per factor); GDN also K^T
             bool slow = false;
-            if (KDA) wait_state();  // the Kinv tile below is the previous state update's operand
+            if (KDA) wait_state();  // the key tile below is the previous state update's operand
             if (KDA) {
-                // [K e^gc ; Q e^gc] (D1's A operand, then the state MMA's) and Kinv = K e^{-gc}
-                // (D1's B operand), rows >= n zero: D1 = [K;Q] K^T with e^{gc_t - gc_i} split as
-                // e^{gc_t} e^{-gc_i}, valid while the chunk's decay e^{-gc_L} stays below e^80
+                // One pass over the chunk's keys and queries, thread per (channel, row part):
+                //  - [K e^gc ; Q e^gc] (D1's A operand, then the state MMA's);
+                //  - Kinv = K e^{-gc} (D1's B operand): D1 = [K;Q] K^T with e^{gc_t - gc_i} split
+                //    as e^{gc_t} e^{-gc_i}, valid while the chunk's decay e^{-gc_L} stays below
+                //    e^80 (else the exact path below);
+                //  - (K e^{gc_L - gc})^T, the state update's key tile, with e^{gc_L - gc} formed
+                //    as e^{gc_L} e^{-gc} (directly where e^{-gc} could overflow).
+                // Rows >= n are zero in all three.
                 const int c = row;
-                const float gLc = sf[SF_GL + c];
-                if (part == NQ - 1 && -gLc > 80.f) *slow_sh = 1;
+                const float gLc = sf[SF_GL + c], eLc = sf[SF_EL + c];
+                const bool steep = -gLc > 80.f;
+                if (part == NQ - 1 && steep) *slow_sh = 1;
+                float kd[4];
 #pragma unroll
                 for (int t = 0; t < C16; ++t) {
                     const int tt = C16 * part + t;
@@ -678,6 +686,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
                     st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
                     st_tf32(sm, w_kr.at(tt), valid ? kv * ei : 0.f);
+                    const float egl = steep ? __expf(gLc - gcr[t]) : eLc * ei;  // <= 1
+                    kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
+                    if ((t & 3) == 3) {
+                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
+                            make_float4(kd[0], kd[1], kd[2], kd[3]);
+                    }
                 }
                 tc::fence_async_smem();
                 __syncthreads();
@@ -693,7 +707,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     for (uint32_t kk = 0; kk < 16; ++kk) {
                         const uint32_t off = (kk & 3u) * 32u;
                         const uint64_t ad = tc::sdesc_sw128((sb + SM_KQG) + (kk >> 2) * 16384u + off);
-                        const uint64_t bd = tc::sdesc_sw128((sb + SM_KDT) + (kk >> 2) * 8192u + off);
+                        const uint64_t bd = tc::sdesc_sw128((sb + SM_P) + (kk >> 2) * 8192u + off);
                         tc::mma_tf32_ss(tm + COL_D1, ad, bd, id, kk > 0);
                     }
                 } else {
@@ -802,7 +816,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             if (!slow) {
                 wait_bar(bar_a, phase_a);
             } else if (KDA) {
-                float *gct = reinterpret_cast<float *>(sm + SM_KDT);  // [64][128] fp32
+                float *gct = reinterpret_cast<float *>(sm + SM_P);  // [64][128] fp32 (Kinv's space)
 #pragma unroll
                 for (int t = 0; t < C16; ++t) gct[(C16 * part + t) * TC_D + row] = gcr[t];
                 __syncthreads();
@@ -832,7 +846,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::fence_after_sync();
             }
             if (!sync_ok(err)) break;
-            if (!KDA && !FRONT && !last) {  // GDN: K|Q tile consumed (D1, K^T, staging)
+            if (!FRONT && !last) {  // K|Q tile consumed (D1, K^T and staging; KDA: the staging
+                                    // pass or the exact D1): the next chunk's in flight
                 if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
                 else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
@@ -893,28 +908,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             tc::fence_before_sync();
             __syncthreads();
 
-            if (KDA) {  // KDA: D1 is complete, its B operand's buffer (or the exact path's gate
-                        // table) is free: (K e^{gc_L - gc})^T, thread per (channel, row part)
-                const int c = row;
-                const float gLc = sf[SF_GL + c];
-                float kd[4];
-#pragma unroll
-                for (int t = 0; t < C16; ++t) {
-                    const int tt = C16 * part + t;
-                    const bool valid = tt < n;
-                    const float kv = ld_bf16(sm, w_kq.at(tt));
-                    const float egl = __expf(gLc - gcr[t]);  // <= 1
-                    kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
-                    if ((t & 3) == 3) {
-                        *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
-                            make_float4(kd[0], kd[1], kd[2], kd[3]);
-                    }
-                }
-                tc::fence_async_smem();
-                tc::fence_before_sync();
-                __syncthreads();
-            }
-
             // ---------------- T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} (the two 32-token
             //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores by
             //   warps 8-15, 4 lanes per column (rows 4m + p); meanwhile warp 0 issues D2. The
@@ -966,20 +959,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             }
             tc::fence_async_smem();
             __syncthreads();
-            if (!last) {  // KDA: K|Q tile consumed by the staging: next chunk's K, Q and gates
-                if (KDA && !FRONT) {
-                    if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
-                    else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
-                    cp_async_commit();
-                }
-                if (KDA) {
-                    const int nn = min(TC_C, len - (ch + 1) * TC_C);
-                    const float *gp = a.g + ((int64_t)(tok0 + TC_C) * Hv + j) * TC_D + row;
+            if (KDA && !last) {  // the next chunk's gates
+                const int nn = min(TC_C, len - (ch + 1) * TC_C);
+                const float *gp = a.g + ((int64_t)(tok0 + TC_C) * Hv + j) * TC_D + row;
 #pragma unroll
-                    for (int t = 0; t < C16; ++t) {
-                        const int tt = C16 * part + t;
-                        pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
-                    }
+                for (int t = 0; t < C16; ++t) {
+                    const int tt = C16 * part + t;
+                    pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
                 }
             }
 
