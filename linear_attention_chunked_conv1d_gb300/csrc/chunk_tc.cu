@@ -573,12 +573,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             const bool last = (ch + 1 == nch);
 
             // ---------------- gates
-            float gcr[KDA ? C16 : 1];  // KDA: gc[C16*part + t][c], c = row
+            // KDA: the cumulative gates in base-2 units, gc[C16*part + t][c] log2(e) (c = row), so
+            // that every decay factor below is one ex2
+            float gcr[KDA ? C16 : 1];
             if (KDA) {
                 float acc = 0.f;
 #pragma unroll
                 for (int t = 0; t < C16; ++t) {
-                    acc += pre_gk[t];
+                    acc = fmaf(pre_gk[t], LOG2E, acc);
                     gcr[t] = acc;
                 }
                 sf[SF_CARRY + part * 128 + row] = acc;
@@ -622,8 +624,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 #pragma unroll
                 for (int t = 0; t < C16; ++t) gcr[t] += carry;
                 if (part == NQ - 1) {
-                    sf[SF_GL + row] = gcr[C16 - 1];
-                    sf[SF_EL + row] = __expf(gcr[C16 - 1]);
+                    sf[SF_GL + row] = gcr[C16 - 1];  // base 2
+                    sf[SF_EL + row] = tc::ex2(gcr[C16 - 1]);
                 }
             } else if (tid < TC_C) {
                 const float gct = sf[SF_GC + tid] + (tid >= 32 ? sf[SF_WARP] : 0.f);
@@ -673,21 +675,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 // Rows >= n are zero in all three.
                 const int c = row;
                 const float gLc = sf[SF_GL + c], eLc = sf[SF_EL + c];
-                const bool steep = -gLc > 80.f;
+                const bool steep = -gLc > 80.f * LOG2E;
                 if (part == NQ - 1 && steep) *slow_sh = 1;
                 float kd[4];
 #pragma unroll
                 for (int t = 0; t < C16; ++t) {
                     const int tt = C16 * part + t;
                     const bool valid = tt < n;
-                    const float kv = ld_bf16(sm, w_kq.at(tt));
-                    const float qv = ld_bf16(sm, w_kq.at(64 + tt));
-                    const float eg = __expf(gcr[t]), ei = __expf(-gcr[t]);
-                    st_tf32(sm, w_kqg.at(tt), valid ? kv * eg : 0.f);
-                    st_tf32(sm, w_kqg.at(64 + tt), valid ? qv * eg : 0.f);
-                    st_tf32(sm, w_kr.at(tt), valid ? kv * ei : 0.f);
-                    const float egl = steep ? __expf(gLc - gcr[t]) : eLc * ei;  // <= 1
-                    kd[t & 3] = tc::to_tf32(valid ? kv * egl : 0.f);
+                    // pad rows are zeroed on input: every factor below is finite (e^{-gc} is
+                    // bounded by e^80 where the product form is used)
+                    const float kv = valid ? ld_bf16(sm, w_kq.at(tt)) : 0.f;
+                    const float qv = valid ? ld_bf16(sm, w_kq.at(64 + tt)) : 0.f;
+                    const float eg = tc::ex2(gcr[t]), ei = tc::ex2(-gcr[t]);
+                    st_tf32(sm, w_kqg.at(tt), kv * eg);
+                    st_tf32(sm, w_kqg.at(64 + tt), qv * eg);
+                    st_tf32(sm, w_kr.at(tt), kv * ei);
+                    const float egl = steep ? tc::ex2(gLc - gcr[t]) : eLc * ei;  // <= 1
+                    kd[t & 3] = tc::to_tf32(kv * egl);
                     if ((t & 3) == 3) {
                         *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
                             make_float4(kd[0], kd[1], kd[2], kd[3]);
@@ -816,7 +820,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             if (!slow) {
                 wait_bar(bar_a, phase_a);
             } else if (KDA) {
-                float *gct = reinterpret_cast<float *>(sm + SM_P);  // [64][128] fp32 (Kinv's space)
+                float *gct = reinterpret_cast<float *>(sm + SM_P);  // [64][128] fp32, base 2 (Kinv's space)
 #pragma unroll
                 for (int t = 0; t < C16; ++t) gct[(C16 * part + t) * TC_D + row] = gcr[t];
                 __syncthreads();
@@ -832,7 +836,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                                 for (int c = 0; c < TC_D; ++c) {
                                     const float lv = ld_bf16(sm, SM_KQ + tc::sw128_offset((isq ? 64 : 0) + r, c, 128, 2));
                                     const float kv = ld_bf16(sm, SM_KQ + tc::sw128_offset(i, c, 128, 2));
-                                    acc = fmaf(lv * kv, __expf(gct[r * TC_D + c] - gct[i * TC_D + c]), acc);
+                                    acc = fmaf(lv * kv, tc::ex2(gct[r * TC_D + c] - gct[i * TC_D + c]), acc);
                                 }
                             }
                             v[ii] = acc;
