@@ -698,11 +698,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     }
                 }
                 tc::fence_async_smem();
+                tc::fence_before_sync();
                 __syncthreads();
                 slow = *slow_sh != 0;
+            } else {
+                tc::fence_before_sync();
+                __syncthreads();
             }
-            tc::fence_before_sync();
-            __syncthreads();
             if (!slow && warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
                 if (KDA) {
