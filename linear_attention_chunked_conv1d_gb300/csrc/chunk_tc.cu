@@ -691,7 +691,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     st_tf32(sm, w_kqg.at(64 + tt), qv * eg);
                     st_tf32(sm, w_kr.at(tt), kv * ei);
                     const float egl = steep ? tc::ex2(gLc - gcr[t]) : eLc * ei;  // <= 1
-                    kd[t & 3] = tc::to_tf32(kv * egl);
+                    kd[t & 3] = tc::to_tf32_operand(kv * egl);
                     if ((t & 3) == 3) {
                         *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, tt - 3, 128, 4)) =
                             make_float4(kd[0], kd[1], kd[2], kd[3]);
@@ -896,8 +896,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4)
                         *reinterpret_cast<float4 *>(sm + SM_P + tc::sw128_offset(r, i0 + q4 * 4, 64, 4)) =
-                            make_float4(tc::to_tf32(v[q4 * 4]), tc::to_tf32(v[q4 * 4 + 1]),
-                                        tc::to_tf32(v[q4 * 4 + 2]), tc::to_tf32(v[q4 * 4 + 3]));
+                            make_float4(tc::to_tf32_operand(v[q4 * 4]), tc::to_tf32_operand(v[q4 * 4 + 1]),
+                                        tc::to_tf32_operand(v[q4 * 4 + 2]), tc::to_tf32_operand(v[q4 * 4 + 3]));
                 } else {
 #pragma unroll
                     for (int ii = 0; ii < 16; ++ii) atp[(i0 + ii) * AT_LD + r] = v[ii];
@@ -905,8 +905,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
                             *reinterpret_cast<float4 *>(sm + SM_NA10 + tc::sw128_offset(r - 32, i0 + q4 * 4, 32, 4)) =
-                                make_float4(tc::to_tf32(-v[q4 * 4]), tc::to_tf32(-v[q4 * 4 + 1]),
-                                            tc::to_tf32(-v[q4 * 4 + 2]), tc::to_tf32(-v[q4 * 4 + 3]));
+                                make_float4(tc::to_tf32_operand(-v[q4 * 4]), tc::to_tf32_operand(-v[q4 * 4 + 1]),
+                                            tc::to_tf32_operand(-v[q4 * 4 + 2]), tc::to_tf32_operand(-v[q4 * 4 + 3]));
                     }
                 }
             }
@@ -1092,8 +1092,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
-                    v[ii] = tc::to_tf32(v[ii]);
-                    w[ii] = KDA ? 0.f : tc::to_tf32(v[ii] * sf[SF_EGL + t0c + ii]);
+                    w[ii] = KDA ? 0.f : tc::to_tf32_operand(v[ii] * sf[SF_EGL + t0c + ii]);
+                    v[ii] = tc::to_tf32_operand(v[ii]);
                 }
                 tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
                 if (!KDA) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RUD + t0c), w);
@@ -1140,10 +1140,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) {
+                for (int ii = 0; ii < 16; ii += 2) {
                     const int t = t0c + ii;
-                    const float o = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
-                    os[t * O_LD + row] = __float2bfloat16_rn(scale * o);
+                    const float o0 = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
+                    const float o1 = KDA ? vq[ii + 1] + vp[ii + 1] : fmaf(sf[SF_EG + t + 1], vq[ii + 1], vp[ii + 1]);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(scale * o0, scale * o1);
+                    os[t * O_LD + row] = pr.x;
+                    os[(t + 1) * O_LD + row] = pr.y;
                 }
                 pend_tok0 = tok0;
                 pend_n = n;

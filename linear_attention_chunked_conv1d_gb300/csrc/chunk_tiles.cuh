@@ -64,8 +64,9 @@ struct ColWalk {
 __device__ __forceinline__ float ld_bf16(const unsigned char *sm, uint32_t off) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off));
 }
+// A tf32 MMA operand element (see tc::to_tf32_operand).
 __device__ __forceinline__ void st_tf32(unsigned char *sm, uint32_t off, float v) {
-    *reinterpret_cast<float *>(sm + off) = tc::to_tf32(v);
+    *reinterpret_cast<float *>(sm + off) = tc::to_tf32_operand(v);
 }
 
 }  // namespace tiles

@@ -271,6 +271,14 @@ __device__ __forceinline__ bool elect_one() {
 __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
+// The same rounding for a value that only ever reaches the tensor core as a tf32 MMA operand:
+// the MMA reads the top 19 bits of the 32-bit pattern and ignores the 13 low ones (a GPU test
+// checks this for operands in shared and in tensor memory), so the add alone rounds and the
+// clearing step is left out. Anything else that reads the value sees it unrounded, low bits
+// and all.
+__device__ __forceinline__ float to_tf32_operand(float x) {
+    return __uint_as_float(__float_as_uint(x) + 0x1000u);
+}
 
 }  // namespace tc
 }  // namespace la

@@ -1,6 +1,6 @@
-// Exhaustive check of la::tc::to_tf32 against the hardware conversion cvt.rna.tf32.f32 over every
-// fp32 bit pattern that is not a NaN: counts the patterns whose results differ and records the
-// smallest one.
+// Exhaustive check of la::tc::to_tf32 (and of la::tc::to_tf32_operand as the tensor core reads
+// it, low 13 bits ignored) against the hardware conversion cvt.rna.tf32.f32 over every fp32 bit
+// pattern that is not a NaN: counts the patterns whose results differ and records the smallest.
 #include <cstdint>
 
 #include "tc.cuh"
@@ -12,9 +12,10 @@ __global__ void round_kernel(unsigned long long *count, unsigned int *first) {
         if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu) != 0u) continue;  // NaN
         const float x = __uint_as_float(b);
         const uint32_t mine = __float_as_uint(la::tc::to_tf32(x));
+        const uint32_t operand = __float_as_uint(la::tc::to_tf32_operand(x)) & 0xFFFFE000u;
         uint32_t ref;
         asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(ref) : "f"(x));
-        if (mine != ref) {
+        if (mine != ref || operand != ref) {
             atomicAdd(count, 1ull);
             atomicMin(first, b);
         }
