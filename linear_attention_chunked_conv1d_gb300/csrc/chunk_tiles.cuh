@@ -61,8 +61,9 @@ struct ColWalk {
     }
 };
 
+// bf16 element widened to fp32 (exact: the bf16 bits are the top half of the fp32 pattern).
 __device__ __forceinline__ float ld_bf16(const unsigned char *sm, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(sm + off));
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(sm + off)) << 16);
 }
 // A tf32 MMA operand element (see tc::to_tf32_operand).
 __device__ __forceinline__ void st_tf32(unsigned char *sm, uint32_t off, float v) {

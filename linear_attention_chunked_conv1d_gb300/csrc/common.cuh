@@ -88,11 +88,22 @@ template <> struct Vec4<__nv_bfloat16> {
 };
 
 __device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) {  // exact widening
+    return __uint_as_float(static_cast<uint32_t>(__bfloat16_as_ushort(x)) << 16);
+}
 template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
+}
+// Two values rounded to T and widened back to fp32 (T = bf16: one paired conversion).
+template <typename T> __device__ __forceinline__ void round_to_2(float &a, float &b);
+template <> __device__ __forceinline__ void round_to_2<float>(float &, float &) {}
+template <> __device__ __forceinline__ void round_to_2<__nv_bfloat16>(float &a, float &b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(&h);
+    a = __uint_as_float(u << 16);
+    b = __uint_as_float(u & 0xFFFF0000u);
 }
 
 // Packed pairs of fp32 (Blackwell f32x2 ALU ops; each lane rounds like the scalar op, so a

@@ -48,12 +48,11 @@ __device__ __forceinline__ void conv_row(const uint64_t (&wp)[K][2], const uint6
     }
     if (HD > 0 && l2_warp) {
         // round to the stored type, then the same reduction as the l2 launch
+        round_to_2<T>(y[0], y[1]);
+        round_to_2<T>(y[2], y[3]);
         float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            y[e] = to_f(from_f<T>(y[e]));
-            ss = fmaf(y[e], y[e], ss);
-        }
+        for (int e = 0; e < 4; ++e) ss = fmaf(y[e], y[e], ss);
 #pragma unroll
         for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         if (do_l2) {
