@@ -813,6 +813,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 wait_state();
             }
 
+            if (KDA && !last) {
+                // the next chunk's gate tile while D1 is computed: 16 loads per thread, 32 KB per
+                // chunk, issued where the SM has nothing else in flight (issued later, with the
+                // loads of every warp at once, they hold the block for about 2.8k cycles)
+                const int nn = min(TC_C, len - (ch + 1) * TC_C);
+                const float *gp = a.g + ((int64_t)(tok0 + TC_C) * Hv + j) * TC_D + row;
+#pragma unroll
+                for (int t = 0; t < C16; ++t) {
+                    const int tt = C16 * part + t;
+                    pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
+                }
+            }
             if (pend_n > 0) {  // previous chunk's output while D1 is computed
                 store_o(pend_tok0, pend_n);
                 pend_n = 0;
@@ -965,15 +977,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             }
             tc::fence_async_smem();
             __syncthreads();
-            if (KDA && !last) {  // the next chunk's gates
-                const int nn = min(TC_C, len - (ch + 1) * TC_C);
-                const float *gp = a.g + ((int64_t)(tok0 + TC_C) * Hv + j) * TC_D + row;
-#pragma unroll
-                for (int t = 0; t < C16; ++t) {
-                    const int tt = C16 * part + t;
-                    pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
-                }
-            }
 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
             wait_bar(bar_b, phase_b);
