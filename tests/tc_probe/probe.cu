@@ -8,7 +8,9 @@
 
 using namespace la::tc;
 
-// mode 0: bf16 A,B from smem; 1: tf32 A,B from smem; 2: tf32 A from TMEM, B from smem
+// mode 0: bf16 A,B from smem; 1: tf32 A,B from smem; 2: tf32 A from TMEM, B from smem;
+// 3: bf16 A from TMEM (two elements per 32-bit column, the lower k in the low half), B bf16
+// from smem
 __global__ void __launch_bounds__(128, 1)
 probe_kernel(const float *A, const float *B, float *D, int N, int K, int mode, int *err) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -17,7 +19,7 @@ probe_kernel(const float *A, const float *B, float *D, int N, int K, int mode, i
     const int M = 128;
     unsigned char *sm = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const bool bf = (mode == 0);
+    const bool bf = (mode == 0 || mode == 3);
     const uint32_t es = bf ? 2 : 4;
     unsigned char *As = sm;
     unsigned char *Bs = sm + M * K * es;
@@ -51,6 +53,17 @@ probe_kernel(const float *A, const float *B, float *D, int N, int K, int mode, i
             tmem_st16(tmem_addr(tbase, lane, 256 + g * 16), v);
         }
         tmem_wait_st();
+    } else if (mode == 3) {
+        for (int g = 0; g < K / 32; ++g) {
+            float v[16];
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 p = __floats2bfloat162_rn(A[tid * K + g * 32 + 2 * i],
+                                                               A[tid * K + g * 32 + 2 * i + 1]);
+                v[i] = *reinterpret_cast<const float *>(&p);
+            }
+            tmem_st16(tmem_addr(tbase, lane, 256 + g * 16), v);
+        }
+        tmem_wait_st();
     }
     fence_async_smem();
     fence_before_sync();
@@ -66,6 +79,8 @@ probe_kernel(const float *A, const float *B, float *D, int N, int K, int mode, i
             const uint64_t bd = sdesc_sw128(smem_u32(Bs) + atom * N * 128 + inner);
             if (mode == 2) {
                 mma_tf32_ts(tbase, tbase + 256 + k0, bd, id, kk > 0);
+            } else if (mode == 3) {
+                mma_bf16_ts(tbase, tbase + 256 + k0 / 2, bd, id, kk > 0);
             } else {
                 const uint64_t ad = sdesc_sw128(smem_u32(As) + atom * M * 128 + inner);
                 if (bf) mma_bf16_ss(tbase, ad, bd, id, kk > 0);

@@ -1,6 +1,7 @@
 """GPU unit check of the tcgen05 helpers (descriptors, instruction descriptors, TMEM
-load/store, MMA from shared and tensor memory) on exactly representable operands, so the
-product must match exactly. Shapes are those the recurrence kernel issues."""
+load/store, MMA from shared and tensor memory, tf32 and bf16, the latter packed two per TMEM
+column when it is the A operand) on exactly representable operands, so the product must match
+exactly. Shapes are those the recurrence kernel issues."""
 import ctypes
 import os
 import subprocess
@@ -32,7 +33,7 @@ def probe(cuda):
 
 @pytest.mark.parametrize("mode,N,K", [(0, 64, 128), (0, 128, 128), (0, 256, 64),
                                       (1, 128, 128), (1, 64, 64), (2, 128, 128), (2, 64, 64),
-                                      (2, 128, 64)])
+                                      (2, 128, 64), (3, 128, 128), (3, 64, 64), (3, 256, 64)])
 def test_tcgen05_mma_exact(probe, cuda, mode, N, K):
     g = torch.Generator("cpu")
     g.manual_seed(mode * 1000 + N + K)
