@@ -64,17 +64,18 @@ constexpr int NQ = TC_THREADS / 128;  // column parts per TMEM lane
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 // TMEM columns. D1 (K K^T | Q K^T) and D6 (U'0^T | Z^T of the block substitution) share
-// columns: D1 is consumed before D6 is produced. V^T (identity MMA) lands in the U'd^T columns
-// before they are reused; K^T (identity MMA, GDN) and then U'1^T land in the P U' accumulator
-// columns before MMA4 overwrites them.
+// columns: D1 is consumed before D6 is produced. K^T (identity MMA, GDN) and then U'1^T land
+// in the P U' accumulator columns before MMA4 overwrites them. V^T (identity MMA, with D2)
+// lands in the U'd^T columns (KDA) or in D1's (GDN, D1 consumed by then); GDN's D2 operand
+// S_hi | S_lo (bf16, two per column) sits in the R^T | U'd^T columns until D2 has read it.
 constexpr uint32_t COL_S = 0, COL_D2 = 128, COL_RU = 256, COL_RUD = 320, COL_D1 = 384,
-                   COL_D6 = 384, COL_D4 = 448;
+                   COL_D6 = 384, COL_D4 = 448, COL_SHI = COL_RU, COL_SLO = COL_RUD;
 constexpr uint32_t TMEM_COLS = 512;
 
 // shared memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t SM_KQ = 0;                    // bf16 SW128 [128 rows: K | Q][128]
 constexpr uint32_t SM_V = SM_KQ + 32768;         // bf16 SW128 [64][128]
-constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: K | Q][128] (KDA: scaled)
+constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: K | Q][128], KDA's decayed tile
 constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t]: K^T (GDN) / Kdec^T (KDA)
 constexpr uint32_t SM_P = SM_KDT + 32768;        // tf32 SW128 [64 t][64 i]
 constexpr uint32_t SM_T00 = SM_P + 16384;        // tf32 SW128 [32 t][32 i]  (I + A00)^{-1}
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
     uint32_t *tmem_sh = reinterpret_cast<uint32_t *>(sm + SM_BARS + 32);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr uint32_t COL_VT = KDA ? COL_RUD : COL_D1;  // V^T from the identity MMA
     const uint32_t lq = tc::tmem_lane_base(warp);  // this warp's TMEM lane quadrant
     // TMEM row (= k-channel c when staging, = v-channel d in the state phases) and which of the
     // NQ parts of the columns (or of the chunk's rows) this thread takes.
@@ -565,7 +567,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             }
         };
         int pend_tok0 = 0, pend_n = 0;  // output tile staged, not yet stored
-        bool staged_ahead = false;      // GDN: the chunk's tf32 K|Q tile is already staged
 
         for (int ch = 0; ch < nch; ++ch) {
             const int tok0 = t0 + ch * TC_C;
@@ -735,82 +736,77 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::mma_commit(bar_a);
             }
 
-            // ---- state-MMA operands. GDN: exact tf32 copy of [K;Q] (the gate factors are
-            //      applied to the MMA results instead). KDA: [K e^gc ; Q e^gc] and
-            //      (K e^{gc_L - gc})^T, thread per (channel, row part).
-            auto stage_state_operands = [&]() {  // GDN
-#pragma unroll
-                for (int m = 0; m < 2048 / TC_THREADS; ++m) {
-                    const int idx = tid + TC_THREADS * m;  // 0..2047 chunks of 8 elements
-                    const int r = idx >> 4, cj = idx & 15;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
-                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        f[2 * e] = __uint_as_float(w4[e] << 16);
-                        f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
-                    }
-                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8, 128, 4)) =
-                        make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8 + 4, 128, 4)) =
-                        make_float4(f[4], f[5], f[6], f[7]);
-                }
-                tc::fence_async_smem();
-            };
-            // the same copy of the next chunk's tile by warps 1-15, while warp 0 runs the
-            // block-substitution chain of this chunk (GDN, separate front end)
-            auto stage_state_operands_ahead = [&]() {
-#pragma unroll
-                for (int m = 0; m < 5; ++m) {
-                    const int idx = (tid - 32) + (TC_THREADS - 32) * m;
-                    if (idx >= 2048) break;
-                    const int r = idx >> 4, cj = idx & 15;
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(sm + SM_KQ + tc::sw128_offset(r, cj * 8, 128, 2));
-                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        f[2 * e] = __uint_as_float(w4[e] << 16);
-                        f[2 * e + 1] = __uint_as_float(w4[e] & 0xFFFF0000u);
-                    }
-                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8, 128, 4)) =
-                        make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4 *>(sm + SM_KQG + tc::sw128_offset(r, cj * 8 + 4, 128, 4)) =
-                        make_float4(f[4], f[5], f[6], f[7]);
-                }
-                tc::fence_async_smem();
-            };
-            // D2 = S [K;Q]^T (tf32, A from TMEM) and V^T (identity MMA) into the U'd columns.
-            // Issued by warp 0 while warps 8-15 solve the triangular blocks: the issuing lane
-            // is held for as long as the tensor core takes to run the group, and warp 0 has no
-            // share in that solve (the barrier before it made the staged operands visible).
+            // D2 = S [K;Q]^T and V^T (identity MMA). KDA: tf32, A (S) from TMEM, B the decayed
+            // [K;Q] tile. GDN: the raw bf16 K|Q tile against S split into two bf16 terms in TMEM
+            // (S = S_hi + S_lo within 2^-18; staged below), two kind::f16 groups accumulating
+            // into D2. Issued by warp 0 while warps 8-15 solve the triangular blocks: the issuing
+            // lane is held for as long as the tensor core takes to run the group, and warp 0 has
+            // no share in that solve (the barrier before it made the staged operands visible).
             auto issue_mma2 = [&]() {
                 if (warp == 0 && tc::elect_one()) {
                     tc::fence_after_sync();
-                    constexpr uint32_t id = tc::idesc(128, 128, tc::FMT_TF32);
+                    if (KDA) {
+                        constexpr uint32_t id = tc::idesc(128, 128, tc::FMT_TF32);
 #pragma unroll
-                    for (uint32_t kk = 0; kk < 16; ++kk) {
-                        const uint64_t bd = tc::sdesc_sw128((sb + SM_KQG) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
-                        tc::mma_tf32_ts(tm + COL_D2, tm + COL_S + kk * 8, bd, id, kk > 0);
+                        for (uint32_t kk = 0; kk < 16; ++kk) {
+                            const uint64_t bd = tc::sdesc_sw128((sb + SM_KQG) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                            tc::mma_tf32_ts(tm + COL_D2, tm + COL_S + kk * 8, bd, id, kk > 0);
+                        }
+                    } else {
+                        constexpr uint32_t id = tc::idesc(128, 128, tc::FMT_BF16);
+#pragma unroll
+                        for (uint32_t h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (uint32_t kk = 0; kk < 8; ++kk) {
+                                const uint64_t bd = tc::sdesc_sw128((sb + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                                tc::mma_bf16_ts(tm + COL_D2, tm + (h ? COL_SLO : COL_SHI) + kk * 8, bd, id,
+                                                (h | kk) > 0);
+                            }
+                        }
                     }
                     constexpr uint32_t idv = tc::idesc(128, 64, tc::FMT_BF16, true, false);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 4; ++kk) {
                         const uint64_t ad = tc::sdesc_sw128_mn((sb + SM_V) + kk * 2048u, 64u * 128u, 1024u);
                         const uint64_t bd = tc::sdesc_sw128((sb + SM_ID) + kk * 32u);
-                        tc::mma_bf16_ss(tm + COL_RUD, ad, bd, idv, kk > 0);
+                        tc::mma_bf16_ss(tm + COL_VT, ad, bd, idv, kk > 0);
                     }
                     tc::mma_commit(bar_b);
                 }
             };
 
-            if (!KDA) {  // GDN: stage while D1 and K^T are computed (unless staged ahead)
-                if (!staged_ahead) stage_state_operands();
-                staged_ahead = false;
+            if (!KDA) {
                 // the previous state update must be complete before the K^T tile below is
-                // rewritten and before D2 reads S
+                // rewritten and before S is read
                 wait_state();
+                // S -> S_hi = bf16(S), S_lo = bf16(S - S_hi), packed two per column, D2's A
+                // operand, while D1 and K^T are computed: thread (lane, part) takes its 32
+                // columns; warp 0 issues D1, so warp 4 (its TMEM lane quadrant) takes its columns
+                auto split_cols = [&](int c0) {  // columns c0 .. c0 + 31 of this warp's lanes
+                    float sv[D32], hi[D32 / 2], lo[D32 / 2];
+#pragma unroll
+                    for (int g = 0; g < D32 / 16; ++g)
+                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < D32 / 2; ++i) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * i], sv[2 * i + 1]);
+                        const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(
+                            sv[2 * i] - __uint_as_float(hu << 16),
+                            sv[2 * i + 1] - __uint_as_float(hu & 0xFFFF0000u));
+                        hi[i] = __uint_as_float(hu);
+                        lo[i] = *reinterpret_cast<const float *>(&l2);
+                    }
+                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_SHI + c0 / 2), hi);
+                    tc::tmem_st16(tc::tmem_addr(tm, lq, COL_SLO + c0 / 2), lo);
+                };
+                if (warp != 0) {
+                    split_cols(D32 * part);
+                    if (warp == 4) split_cols(0);
+                    tc::tmem_wait_st();
+                    tc::fence_before_sync();
+                }
             }
 
             if (KDA && !last) {
@@ -864,8 +860,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::fence_after_sync();
             }
             if (!sync_ok(err)) break;
-            if (!FRONT && !last) {  // K|Q tile consumed (D1, K^T and staging; KDA: the staging
-                                    // pass or the exact D1): the next chunk's in flight
+            if (KDA && !FRONT && !last) {  // KDA: K|Q tile consumed (the staging pass or the
+                                           // exact D1): the next chunk's in flight
                 if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
                 else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
@@ -981,8 +977,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
-            if (!last) {  // V tile consumed by the identity MMA: next chunk's V (FRONT: the
-                          // raw rows, into the tf32 K|Q buffer the state MMA has read) in flight
+            if (!last) {  // V tile consumed by the identity MMA (GDN: the K|Q tile by D2 too):
+                          // the next chunk's in flight (FRONT: the raw rows, into the tf32 K|Q
+                          // buffer, which D2 has read)
+                if (!KDA && !FRONT) {
+                    if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
+                    else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+                }
                 if (FRONT) load_raw(a, sm, nullptr, t0, len, (ch + 1) * TC_C, kh, j, tid);
                 else if (use_tma && !alt) tma_v(j, tok0 + TC_C);
                 else load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid, alt);
@@ -992,7 +993,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 const int t0c = C16 * part;
                 float v[16], vt[16];
                 tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + t0c), v);
-                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_RUD + t0c), vt);
+                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_VT + t0c), vt);
                 tc::tmem_wait_ld();
 #pragma unroll
                 for (int ii = 0; ii < 16; ++ii) {
@@ -1003,14 +1004,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
                 if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);  // Z = R1
                 tc::tmem_wait_st();
-            }
-            // GDN, separate front end: the next chunk's K|Q copies (issued once D1 was read;
-            // the V copies just issued may stay in flight) have landed for every thread after
-            // the barrier below, and its tf32 copy can be staged during the chain
-            const bool stage_ahead = !KDA && !FRONT && !last;
-            if (stage_ahead) {
-                if (use_tma && !alt) tma_wait(bar_kq, par_kq);  // the next chunk's K|Q
-                else cp_async_wait_but_last();
             }
             tc::fence_before_sync();
             __syncthreads();
@@ -1078,10 +1071,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + cs), sx);
                 }
                 tc::tmem_wait_st();
-            }
-            if (stage_ahead) {  // the D2 MMA of this chunk, the tile's one reader, is complete
-                if (warp != 0) stage_state_operands_ahead();
-                staged_ahead = true;
             }
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
