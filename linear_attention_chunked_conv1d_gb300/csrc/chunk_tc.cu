@@ -88,7 +88,7 @@ constexpr uint32_t O_LD = 136;                   // padded row (bf16) of the out
 constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_LD * 4;
 // small region (floats)
 constexpr uint32_t SF_GC = 0, SF_GC2 = 64, SF_BETA = 128, SF_EG = 192, SF_EGL = 256,
-                   SF_GL = 320, SF_EL = 448, SF_GM = 576, SF_CARRY = 704 /* [NQ][128] */,
+                   SF_GL = 320, SF_EL = 448, SF_CARRY = 704 /* [NQ][128] */,
                    SF_WARP = 704 + 128 * NQ, SF_RF = SF_WARP + 8, SF_CF = SF_RF + 64,
                    SF_END = SF_CF + 64;
 constexpr uint32_t SM_BARS = SM_SMALL + SF_END * 4;  // mbarriers, flags, tmem base (128 B)
