@@ -10,6 +10,7 @@ using namespace la::tc;
 
 // mode 1: bf16, A K-major [128][K] smem, B MN-major [K][N]
 // mode 2: bf16, A MN-major [K][128] smem, B K-major [N][K]
+// mode 4: bf16, A in TMEM (two per column), B MN-major [K][N]
 // Bt / At are given row-major as [K][N] / [K][128].
 __global__ void __launch_bounds__(128, 1)
 probe_mn_kernel(const float *A, const float *B, float *D, int N, int K, int mode, int swap,
@@ -24,7 +25,7 @@ probe_mn_kernel(const float *A, const float *B, float *D, int N, int K, int mode
     unsigned char *As = sm;
     unsigned char *Bs = sm + M * K * es;
     // A: mode 1 K-major [128][K]; mode 2 MN-major stored as tile [K rows][128 cols]
-    if (mode == 1) {
+    if (mode == 1 || mode == 4) {
         for (int i = tid; i < M * K; i += 128) {
             int r = i / K, k = i % K;
             *(__nv_bfloat16 *)(As + sw128_offset(r, k, M, 2)) = __float2bfloat16_rn(A[i]);
@@ -59,6 +60,18 @@ probe_mn_kernel(const float *A, const float *B, float *D, int N, int K, int mode
     fence_after_sync();
     const uint32_t tbase = tmem_base_sh;
     const uint32_t lane = tmem_lane_base(warp);
+    if (mode == 4) {  // A row tid -> TMEM lane tid, columns 256.. (packed pairs)
+        for (int g = 0; g < K / 32; ++g) {
+            float v[16];
+            for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 p = __floats2bfloat162_rn(A[tid * K + g * 32 + 2 * i],
+                                                               A[tid * K + g * 32 + 2 * i + 1]);
+                v[i] = *reinterpret_cast<const float *>(&p);
+            }
+            tmem_st16(tmem_addr(tbase, lane, 256 + g * 16), v);
+        }
+        tmem_wait_st();
+    }
     fence_async_smem();
     fence_before_sync();
     __syncthreads();
@@ -69,7 +82,12 @@ probe_mn_kernel(const float *A, const float *B, float *D, int N, int K, int mode
         // along K 1024 bytes apart. swap exchanges the two offsets (to detect a misreading).
         for (uint32_t kk = 0; kk < (uint32_t)K / kstep; ++kk) {
             const uint32_t k0 = kk * kstep;
-            if (mode == 1) {
+            if (mode == 4) {
+                uint32_t lbo = K * 128, sbo = 1024;
+                if (swap) { uint32_t t = lbo; lbo = sbo; sbo = t; }
+                const uint64_t bd = sdesc_sw128_mn(smem_u32(Bs) + k0 * 128, lbo, sbo);
+                mma_bf16_ts(tbase, tbase + 256 + k0 / 2, bd, idesc(M, N, FMT_BF16, false, true), kk > 0);
+            } else if (mode == 1) {
                 uint32_t lbo = K * 128, sbo = 1024;
                 if (swap) { uint32_t t = lbo; lbo = sbo; sbo = t; }
                 const uint32_t per_atom = 64, atom = k0 / per_atom, inner = (k0 % per_atom) * 2;
@@ -106,7 +124,7 @@ probe_mn_kernel(const float *A, const float *B, float *D, int N, int K, int mode
 
 extern "C" int probe_mn_run(const float *A, const float *B, float *D, int N, int K, int mode,
                             int swap, int *err) {
-    if (mode != 1 && mode != 2) return -4;
+    if (mode != 1 && mode != 2 && mode != 4) return -4;
     const size_t es = 2;
     const size_t smem = (128 + N) * K * es + 1024;
     if (cudaFuncSetAttribute(probe_mn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

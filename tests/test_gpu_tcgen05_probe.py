@@ -66,8 +66,10 @@ def _mn_run(probe, cuda, mode, N, K, swap):
     return torch.equal(D.cpu(), ref)
 
 
-@pytest.mark.parametrize("mode,N,K", [(1, 128, 64), (1, 64, 128), (2, 64, 128), (2, 128, 64)])
+@pytest.mark.parametrize("mode,N,K", [(1, 128, 64), (1, 64, 128), (2, 64, 128), (2, 128, 64),
+                                      (4, 128, 64), (4, 64, 128)])
 def test_tcgen05_mma_mn_major_bf16(probe, cuda, mode, N, K):
-    """bf16 MN-major operand: leading byte offset = distance between 128-byte atoms along M/N,
-    stride byte offset = distance between 8-row groups along K."""
+    """bf16 MN-major operand (mode 4: with A in tensor memory): leading byte offset = distance
+    between 128-byte atoms along M/N, stride byte offset = distance between 8-row groups along
+    K."""
     assert _mn_run(probe, cuda, mode, N, K, swap=0)
