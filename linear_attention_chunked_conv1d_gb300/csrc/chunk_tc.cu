@@ -64,10 +64,11 @@ constexpr int NQ = TC_THREADS / 128;  // column parts per TMEM lane
 constexpr uint64_t WAIT_NS = 2000000000ull;
 
 // TMEM columns. D1 (K K^T | Q K^T) and D6 (U'0^T | Z^T of the block substitution) share
-// columns: D1 is consumed before D6 is produced. K^T (identity MMA, GDN) and then U'1^T land
-// in the P U' accumulator columns before MMA4 overwrites them. V^T (identity MMA, with D2)
-// lands in the U'd^T columns (KDA) or in D1's (GDN, D1 consumed by then); GDN's D2 operand
-// S_hi | S_lo (bf16, two per column) sits in the R^T | U'd^T columns until D2 has read it.
+// columns: D1 is consumed before D6 is produced. U'1^T lands in the P U' accumulator columns
+// before MMA4 overwrites them. V^T (identity MMA, with D2) lands in the U'd^T columns (KDA) or
+// in D1's (GDN, D1 consumed by then); GDN's D2 operand S_hi | S_lo (bf16, two per column) sits
+// in the R^T | U'd^T columns until D2 has read it, and its state-update operand Ud_hi | Ud_lo
+// in the U'd^T columns.
 constexpr uint32_t COL_S = 0, COL_D2 = 128, COL_RU = 256, COL_RUD = 320, COL_D1 = 384,
                    COL_D6 = 384, COL_D4 = 448, COL_SHI = COL_RU, COL_SLO = COL_RUD;
 constexpr uint32_t TMEM_COLS = 512;
@@ -76,7 +77,8 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SM_KQ = 0;                    // bf16 SW128 [128 rows: K | Q][128]
 constexpr uint32_t SM_V = SM_KQ + 32768;         // bf16 SW128 [64][128]
 constexpr uint32_t SM_KQG = SM_V + 16384;        // tf32 SW128 [128 rows: K | Q][128], KDA's decayed tile
-constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t]: K^T (GDN) / Kdec^T (KDA)
+constexpr uint32_t SM_KDT = SM_KQG + 65536;      // tf32 SW128 [128 c][64 t]: Kdec^T (KDA)
+constexpr uint32_t SM_KQ1 = SM_KDT;              // GDN: the K|Q tile of odd chunks (bf16, as SM_KQ)
 constexpr uint32_t SM_P = SM_KDT + 32768;        // tf32 SW128 [64 t][64 i]
 constexpr uint32_t SM_T00 = SM_P + 16384;        // tf32 SW128 [32 t][32 i]  (I + A00)^{-1}
 constexpr uint32_t SM_T11 = SM_T00 + 4096;       // tf32 SW128 [32 t][32 i]  (I + A11)^{-1}
@@ -120,10 +122,10 @@ struct TcParams {
 // Issue the K, Q (k-head kh) and V (v-head j) rows of one chunk as 16-byte async copies into
 // the swizzled tiles; rows >= n are zero-filled (their source is never read).
 __device__ __forceinline__ void load_kq(const RecArgs &a, unsigned char *sm, int tok0, int n,
-                                        int kh, int tid) {
+                                        int kh, int tid, uint32_t kqo = SM_KQ) {
     const __nv_bfloat16 *kp = reinterpret_cast<const __nv_bfloat16 *>(a.k) + (int64_t)kh * TC_D;
     const __nv_bfloat16 *qp = reinterpret_cast<const __nv_bfloat16 *>(a.q) + (int64_t)kh * TC_D;
-    const uint32_t base = tc::smem_u32(sm + SM_KQ);
+    const uint32_t base = tc::smem_u32(sm + kqo);
 #pragma unroll
     for (int m = 0; m < 2048 / TC_THREADS; ++m) {
         const int idx = tid + TC_THREADS * m;  // 0..2047
@@ -222,7 +224,7 @@ __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
 // or zero (v). K4: a 4-tap conv (no leading zero taps to skip).
 template <bool K4>
 __device__ __forceinline__ void conv_tile(const RecArgs &a, unsigned char *sm, int n, float pad,
-                                          int warp, int lane) {
+                                          int warp, int lane, uint32_t kqo) {
     const float *cw = reinterpret_cast<const float *>(sm + SM_CW);
     const float *cb = reinterpret_cast<const float *>(sm + SM_CB);
     const int m0 = K4 ? 0 : 4 - a.conv_k;  // first tap that is not zero
@@ -286,15 +288,15 @@ __device__ __forceinline__ void conv_tile(const RecArgs &a, unsigned char *sm, i
                                       *reinterpret_cast<const uint32_t *>(&hi));
             if (tau >= n) packed = sec < 2 ? make_uint2(pfw, pfw) : make_uint2(0u, 0u);
             const uint32_t off = sec == 2 ? SM_V + tc::sw128_offset(tau, 4 * lane, 64, 2)
-                                          : SM_KQ + tc::sw128_offset((sec == 0 ? 64 : 0) + tau, 4 * lane, 128, 2);
+                                          : kqo + tc::sw128_offset((sec == 0 ? 64 : 0) + tau, 4 * lane, 128, 2);
             *reinterpret_cast<uint2 *>(sm + off) = packed;
         }
     }
 }
 __device__ __forceinline__ void conv_tile_any(const RecArgs &a, unsigned char *sm, int n,
-                                              float pad, int warp, int lane) {
-    if (a.conv_k == 4) conv_tile<true>(a, sm, n, pad, warp, lane);
-    else conv_tile<false>(a, sm, n, pad, warp, lane);
+                                              float pad, int warp, int lane, uint32_t kqo) {
+    if (a.conv_k == 4) conv_tile<true>(a, sm, n, pad, warp, lane, kqo);
+    else conv_tile<false>(a, sm, n, pad, warp, lane, kqo);
 }
 
 // New conv state of a stream, rows i < kernel - 1 = stream rows len - (kernel - 1) + i of
@@ -414,15 +416,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
     const bool use_tma = !FRONT && P.tma != 0;
     uint32_t par_kq = 0, par_v = 0;
     bool fly_kq = false, fly_v = false;
-    auto tma_kq = [&](int kh_, int tok) {
+    auto tma_kq = [&](int kh_, int tok, uint32_t kqo) {
         if (tid == 0) {
             tc::fence_async_smem();  // earlier generic accesses of the tile come first
             tc::mbar_expect_tx(bar_kq, 32768u);
             const int x = kh_ * TC_D;
-            tc::tma_load_2d(sb + SM_KQ, &P.map_k, x, tok, bar_kq);           // K, channels 0-63
-            tc::tma_load_2d(sb + SM_KQ + 16384, &P.map_k, x + 64, tok, bar_kq);  // K, 64-127
-            tc::tma_load_2d(sb + SM_KQ + 8192, &P.map_q, x, tok, bar_kq);    // Q rows 64.. of the tile
-            tc::tma_load_2d(sb + SM_KQ + 24576, &P.map_q, x + 64, tok, bar_kq);
+            tc::tma_load_2d(sb + kqo, &P.map_k, x, tok, bar_kq);           // K, channels 0-63
+            tc::tma_load_2d(sb + kqo + 16384, &P.map_k, x + 64, tok, bar_kq);  // K, 64-127
+            tc::tma_load_2d(sb + kqo + 8192, &P.map_q, x, tok, bar_kq);    // Q rows 64.. of the tile
+            tc::tma_load_2d(sb + kqo + 24576, &P.map_q, x + 64, tok, bar_kq);
             fly_kq = true;
         }
     };
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             load_conv_weights(a, sm, kh, j, tid);
             load_raw(a, sm, conv_state, t0, len, 0, kh, j, tid);
         } else if (use_tma && !alt) {
-            tma_kq(kh, t0);
+            tma_kq(kh, t0, SM_KQ);
             tma_v(j, t0);
         } else {
             load_kq(a, sm, t0, min(TC_C, len), kh, tid);
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 __syncthreads();
                 write_conv_state(a, sm, conv_state, t0, len, kh, j, *qk_sh ? 0 : 2, 3, tid);
             }
-            conv_tile_any(a, sm, min(TC_C, len), pad_qk, warp, lane);
+            conv_tile_any(a, sm, min(TC_C, len), pad_qk, warp, lane, SM_KQ);
             tc::fence_async_smem();
         }
 
@@ -572,6 +574,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             const int tok0 = t0 + ch * TC_C;
             const int n = min(TC_C, len - ch * TC_C);
             const bool last = (ch + 1 == nch);
+            // K|Q tile of this chunk and of the next: GDN alternates two buffers by chunk parity
+            // (the state update reads the tile at the end of the chunk, after the next one's
+            // load has been issued); KDA reads it only until D1 and keeps one
+            const uint32_t kqo = (KDA || !(ch & 1)) ? SM_KQ : SM_KQ1;
+            const uint32_t kqo_next = (KDA || (ch & 1)) ? SM_KQ : SM_KQ1;
 
             // ---------------- gates
             // KDA: the cumulative gates in base-2 units, gc[C16*part + t][c] log2(e) (c = row), so
@@ -642,8 +649,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 const __nv_bfloat16 pf = __float2bfloat16_rn(a.pad_fill);
                 for (int idx = tid; idx < (TC_C - n) * TC_D; idx += TC_THREADS) {
                     const int r = n + idx / TC_D, c = idx % TC_D;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(r, c, 128, 2)) = pf;
-                    *reinterpret_cast<__nv_bfloat16 *>(sm + SM_KQ + tc::sw128_offset(64 + r, c, 128, 2)) = pf;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + kqo + tc::sw128_offset(r, c, 128, 2)) = pf;
+                    *reinterpret_cast<__nv_bfloat16 *>(sm + kqo + tc::sw128_offset(64 + r, c, 128, 2)) = pf;
                     if (use_tma && !alt)
                         *reinterpret_cast<__nv_bfloat16 *>(sm + SM_V + tc::sw128_offset(r, c, 64, 2)) =
                             __float2bfloat16_rn(0.f);
@@ -721,16 +728,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     constexpr uint32_t id = tc::idesc(128, 64, tc::FMT_BF16);
 #pragma unroll
                     for (uint32_t kk = 0; kk < 8; ++kk) {
-                        const uint32_t addr = (sb + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u;
+                        const uint32_t addr = (sb + kqo) + (kk >> 2) * 16384u + (kk & 3u) * 32u;
                         tc::mma_bf16_ss(tm + COL_D1, tc::sdesc_sw128(addr), tc::sdesc_sw128(addr), id, kk > 0);
-                    }
-                    // K^T[c][t] = sum_i K[i][c] I[t][i]: A = K tile read MN-major
-                    constexpr uint32_t idt = tc::idesc(128, 64, tc::FMT_BF16, true, false);
-#pragma unroll
-                    for (uint32_t kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = tc::sdesc_sw128_mn((sb + SM_KQ) + kk * 2048u, 128u * 128u, 1024u);
-                        const uint64_t bd = tc::sdesc_sw128((sb + SM_ID) + kk * 32u);
-                        tc::mma_bf16_ss(tm + COL_D4, ad, bd, idt, kk > 0);
                     }
                 }
                 tc::mma_commit(bar_a);
@@ -758,7 +757,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                         for (uint32_t h = 0; h < 2; ++h) {
 #pragma unroll
                             for (uint32_t kk = 0; kk < 8; ++kk) {
-                                const uint64_t bd = tc::sdesc_sw128((sb + SM_KQ) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                                const uint64_t bd = tc::sdesc_sw128((sb + kqo) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
                                 tc::mma_bf16_ts(tm + COL_D2, tm + (h ? COL_SLO : COL_SHI) + kk * 8, bd, id,
                                                 (h | kk) > 0);
                             }
@@ -776,9 +775,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             };
 
             if (!KDA) {
-                // the previous state update must be complete before the K^T tile below is
-                // rewritten and before S is read
+                // the previous state update is complete: S may be read, and the K|Q buffer it
+                // read takes the next chunk's tile
                 wait_state();
+                if (!FRONT && !last) {
+                    if (use_tma && !alt) tma_kq(kh, tok0 + TC_C, kqo_next);
+                    else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid, kqo_next);
+                    cp_async_commit();
+                }
                 // S -> S_hi = bf16(S), S_lo = bf16(S - S_hi), packed two per column, D2's A
                 // operand, while D1 and K^T are computed: thread (lane, part) takes its 32
                 // columns; warp 0 issues D1, so warp 4 (its TMEM lane quadrant) takes its columns
@@ -862,7 +866,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             if (!sync_ok(err)) break;
             if (KDA && !FRONT && !last) {  // KDA: K|Q tile consumed (the staging pass or the
                                            // exact D1): the next chunk's in flight
-                if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
+                if (use_tma && !alt) tma_kq(kh, tok0 + TC_C, SM_KQ);
                 else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
             }
@@ -951,25 +955,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     st_tf32(sm, tile + tc::sw128_offset(4 * m + p, jj, 32, 4), x[m]);
             } else {
                 if (warp == 0) issue_mma2();
-                if (!KDA) {
-                    // K^T[c][t] (exact in tf32) -> the [c][t] tile, columns t >= n zeroed: warps
-                    // 0-7, two 16-column groups per thread (the solve leaves them idle)
-                    const int c = row;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int i0 = 16 * (warp >> 2) + 32 * h;
-                        float kt[16];
-                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + i0), kt);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int t = i0 + q4 * 4;
-                            *reinterpret_cast<float4 *>(sm + SM_KDT + tc::sw128_offset(c, t, 128, 4)) =
-                                make_float4(t + 0 < n ? kt[q4 * 4 + 0] : 0.f, t + 1 < n ? kt[q4 * 4 + 1] : 0.f,
-                                            t + 2 < n ? kt[q4 * 4 + 2] : 0.f, t + 3 < n ? kt[q4 * 4 + 3] : 0.f);
-                        }
-                    }
-                }
             }
             tc::fence_async_smem();
             __syncthreads();
@@ -977,13 +962,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
-            if (!last) {  // V tile consumed by the identity MMA (GDN: the K|Q tile by D2 too):
-                          // the next chunk's in flight (FRONT: the raw rows, into the tf32 K|Q
-                          // buffer, which D2 has read)
-                if (!KDA && !FRONT) {
-                    if (use_tma && !alt) tma_kq(kh, tok0 + TC_C);
-                    else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
-                }
+            if (!last) {  // V tile consumed by the identity MMA: the next chunk's in flight (FRONT:
+                          // the raw rows, into the tf32 K|Q buffer, which D2 has read)
                 if (FRONT) load_raw(a, sm, nullptr, t0, len, (ch + 1) * TC_C, kh, j, tid);
                 else if (use_tma && !alt) tma_v(j, tok0 + TC_C);
                 else load_v(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), j, tid, alt);
@@ -1075,48 +1055,75 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             wait_bar(bar_b, phase_b);
             if (!sync_ok(err)) break;
 
-            // ------ U'^T -> TMEM (tf32); GDN also U'^T diag(e^{gc_L - gc}) for the state update
+            // ------ U'^T -> TMEM (tf32); GDN also Ud^T = U'^T diag(e^{gc_L - gc}) for the state
+            //        update, as two bf16 terms (Ud = Ud_hi + Ud_lo within 2^-18) packed two per
+            //        column: hi in the U'd columns 0..31, lo in 32..63
             {
                 const int t0c = C16 * part;  // 16 columns: U'0 (in D6) or U'1 (in D4)
-                float v[16], w[16];
+                float v[16];
                 if (t0c < 32) tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);
                 else tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c - 32), v);
                 tc::tmem_wait_ld();
+                if (!KDA) {
+                    float hi[8], lo[8];
 #pragma unroll
-                for (int ii = 0; ii < 16; ++ii) {
-                    w[ii] = KDA ? 0.f : tc::to_tf32_operand(v[ii] * sf[SF_EGL + t0c + ii]);
-                    v[ii] = tc::to_tf32_operand(v[ii]);
+                    for (int i = 0; i < 8; ++i) {
+                        const float w0 = v[2 * i] * sf[SF_EGL + t0c + 2 * i];
+                        const float w1 = v[2 * i + 1] * sf[SF_EGL + t0c + 2 * i + 1];
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(w0, w1);
+                        const uint32_t hu = *reinterpret_cast<const uint32_t *>(&h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(w0 - __uint_as_float(hu << 16),
+                                                                        w1 - __uint_as_float(hu & 0xFFFF0000u));
+                        hi[i] = __uint_as_float(hu);
+                        lo[i] = *reinterpret_cast<const float *>(&l2);
+                    }
+                    tc::tmem_st8(tc::tmem_addr(tm, lq, COL_RUD + t0c / 2), hi);
+                    tc::tmem_st8(tc::tmem_addr(tm, lq, COL_RUD + 32 + t0c / 2), lo);
                 }
+#pragma unroll
+                for (int ii = 0; ii < 16; ++ii) v[ii] = tc::to_tf32_operand(v[ii]);
                 tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RU + t0c), v);
-                if (!KDA) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_RUD + t0c), w);
             }
             tc::tmem_wait_st();
             if (FRONT && !last) cp_async_wait_all();  // next chunk's raw rows
             tc::fence_before_sync();
             __syncthreads();
 
-            // ---------------- D4 = U'^T P^T ; S += U'd^T K (GDN) or U'^T Kdec (KDA)
+            // ---------------- D4 = U'^T P^T ; S += Ud^T K (GDN) or U'^T Kdec (KDA)
             if (warp == 0 && tc::elect_one()) {
                 tc::fence_after_sync();
                 constexpr uint32_t id64 = tc::idesc(128, 64, tc::FMT_TF32);
-                constexpr uint32_t id128 = tc::idesc(128, 128, tc::FMT_TF32);
 #pragma unroll
                 for (uint32_t kk = 0; kk < 8; ++kk) {
                     const uint64_t bp = tc::sdesc_sw128((sb + SM_P) + (kk >> 2) * 8192u + (kk & 3u) * 32u);
                     tc::mma_tf32_ts(tm + COL_D4, tm + COL_RU + kk * 8, bp, id64, kk > 0);
                 }
                 tc::mma_commit(bar_b);  // the output MMA: the epilogue may start
-                const uint32_t a5 = KDA ? COL_RU : COL_RUD;
+                if (KDA) {
+                    constexpr uint32_t id128 = tc::idesc(128, 128, tc::FMT_TF32);
 #pragma unroll
-                for (uint32_t kk = 0; kk < 8; ++kk) {
-                    const uint64_t bk = tc::sdesc_sw128((sb + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
-                    tc::mma_tf32_ts(tm + COL_S, tm + a5 + kk * 8, bk, id128, 1);
+                    for (uint32_t kk = 0; kk < 8; ++kk) {
+                        const uint64_t bk = tc::sdesc_sw128((sb + SM_KDT) + (kk >> 2) * 16384u + (kk & 3u) * 32u);
+                        tc::mma_tf32_ts(tm + COL_S, tm + COL_RU + kk * 8, bk, id128, 1);
+                    }
+                } else {
+                    // B = the chunk's K rows [t][c] read MN-major (two 64-channel atoms 16 KB
+                    // apart, 8-token groups 1024 bytes apart); A = Ud_hi, then Ud_lo
+                    constexpr uint32_t idk = tc::idesc(128, 128, tc::FMT_BF16, false, true);
+#pragma unroll
+                    for (uint32_t h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (uint32_t kk = 0; kk < 4; ++kk) {
+                            const uint64_t bk = tc::sdesc_sw128_mn((sb + kqo) + kk * 2048u, 128u * 128u, 1024u);
+                            tc::mma_bf16_ts(tm + COL_S, tm + COL_RUD + 32 * h + kk * 8, bk, idk, 1);
+                        }
+                    }
                 }
                 tc::mma_commit(bar_c);
             }
             pend_c = true;
             if (FRONT && !last) {  // next chunk's q, k, v tiles while the tensor core works
-                conv_tile_any(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane);
+                conv_tile_any(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane, kqo_next);
                 tc::fence_async_smem();
             }
             wait_bar(bar_b, phase_b);
