@@ -15,11 +15,15 @@
 //                                        [K e^gc ; Q e^gc] (K e^{-gc})^T)
 //   A  = strictly-lower(beta_t e^{gc_t-gc_i} D1_KK),  P = lower(e^{gc_t-gc_i} D1_QK)
 //   T  = (I + A)^{-1}                    CUDA cores, forward substitution per column
-//   D2 = S [K e^gc ; Q e^gc]^T           tensor core (tf32, A operand read from TMEM)
+//   D2 = S [K e^gc ; Q e^gc]^T           tensor core (KDA: tf32, S read from TMEM; GDN: S as
+//                                        two bf16 terms in TMEM against the raw bf16 tile,
+//                                        the decays applied to the result)
 //   R^T = beta (V^T - D2[:, :64])        CUDA cores -> TMEM
 //   U'^T = R^T T^T                       tensor core
-//   O^T = D2[:, 64:] + U'^T P^T          tensor core, accumulating into D2
+//   O^T = D2[:, 64:] + U'^T P^T          tensor core (U'^T P^T), summed in the epilogue
 //   S  <- S diag(e^{gc_L}) + U'^T (K e^{gc_L - gc})     tensor core, accumulating into S
+//                                        (GDN: Ud = U' e^{gc_L - gc} as two bf16 terms
+//                                        against the raw K rows)
 //   o  = scale O                          epilogue
 // which is the token recurrence S_t = S_{t-1} diag(a_t)(I - b_t k_t k_t^T) + b_t v_t k_t^T,
 // o_t = scale S_t q_t, unrolled over the chunk. Every exponent is <= 0 except the two split
@@ -31,8 +35,8 @@
 // the pre-conv rows x — causal depthwise conv over the carried conv state, SiLU, and the L2
 // norm of each q and k row ("glm5next_kda/prefill.rs", conv_prefill and l2 launches) — so the
 // conv output never reaches HBM. The next chunk's raw rows (64 + 3 halo) are copied into the
-// buffer of the tf32 K|Q tile once the state MMA has read it, and turned into the bf16 tiles
-// while the tensor core runs the state update. Arithmetic and reduction order are those of
+// buffer of the tf32 K|Q tile once D2 has read it, and turned into the bf16 tiles while the
+// tensor core runs the state update. Arithmetic and reduction order are those of
 // the conv and L2 kernels, so both paths give identical bits. The conv state of a stream is
 // advanced by the blocks that read it: v channels by their unit, q|k channels by the last of
 // the units sharing that k-head to read the old state (a per-(stream, k-head) count).
@@ -40,7 +44,8 @@
 // Precision: operands that are raw bf16 inputs use kind::f16; operands derived from fp32
 // values (state, T, U', decayed keys) use kind::tf32 with round-to-nearest conversion, except
 // the two intermediate products of the block substitution (U'0 and Z, inside U' = R T^T),
-// which the next MMA reads from TMEM without that rounding step;
+// which the next MMA reads from TMEM without that rounding step, and GDN's state and Ud, which
+// enter kind::f16 MMAs as two bf16 terms each (within 2^-18 of the fp32 value);
 // accumulation is fp32. Rows at or past a stream's end are removed by selects.
 #include <cuda.h>
 
@@ -669,7 +674,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 sf[SF_CF + tid] = __expf(gm - gct);
             }
 
-            // ---------------- D1 = [K;Q] K^T (KDA: tf32, decays split per factor); GDN also K^T
+            // ---------------- D1 = [K;Q] K^T (KDA: tf32, decays split per factor)
             bool slow = false;
             if (KDA) wait_state();  // the key tile below is the previous state update's operand
             if (KDA) {
@@ -784,7 +789,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     cp_async_commit();
                 }
                 // S -> S_hi = bf16(S), S_lo = bf16(S - S_hi), packed two per column, D2's A
-                // operand, while D1 and K^T are computed: thread (lane, part) takes its 32
+                // operand, while D1 is computed: thread (lane, part) takes its 32
                 // columns; warp 0 issues D1, so warp 4 (its TMEM lane quadrant) takes its columns
                 auto split_cols = [&](int c0) {  // columns c0 .. c0 + 31 of this warp's lanes
                     float sv[D32], hi[D32 / 2], lo[D32 / 2];
