@@ -1,5 +1,5 @@
 // Host-side TMA tensor-map encoding for the kernels that load tiles with
-// cp.async.bulk.tensor (the projection GEMM).
+// cp.async.bulk.tensor (the projection GEMM; the recurrence's K, Q and V tiles).
 #include <cuda.h>
 
 #include <mutex>
