@@ -965,8 +965,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             __syncthreads();
 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
+            // every thread reads D2 and V^T only after its own wait, and this phase writes no
+            // shared memory: a timed-out wait is caught at the next checked barrier
             wait_bar(bar_b, phase_b);
-            if (!sync_ok(err)) break;
             if (!last) {  // V tile consumed by the identity MMA: the next chunk's in flight (FRONT:
                           // the raw rows, into the tf32 K|Q buffer, which D2 has read)
                 if (FRONT) load_raw(a, sm, nullptr, t0, len, (ch + 1) * TC_C, kh, j, tid);
@@ -1057,8 +1058,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 }
                 tc::tmem_wait_st();
             }
-            wait_bar(bar_b, phase_b);
-            if (!sync_ok(err)) break;
+            wait_bar(bar_b, phase_b);  // each thread reads the chain's results after its own wait
 
             // ------ U'^T -> TMEM (tf32); GDN also Ud^T = U'^T diag(e^{gc_L - gc}) for the state
             //        update, as two bf16 terms (Ud = Ud_hi + Ud_lo within 2^-18) packed two per
@@ -1131,8 +1131,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 conv_tile_any(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane, kqo_next);
                 tc::fence_async_smem();
             }
-            wait_bar(bar_b, phase_b);
-            if (!sync_ok(err)) break;
+            wait_bar(bar_b, phase_b);  // each thread reads D4 after its own wait
 
             // ---------------- o = scale (e^gc (Q H) + P U'): staged as bf16 [t][d] in shared
             //                  memory; written with 16-byte stores (rows < n) in the next chunk
