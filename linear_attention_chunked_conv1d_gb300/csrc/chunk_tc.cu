@@ -961,8 +961,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             } else {
                 if (warp == 0) issue_mma2();
             }
+            // the T blocks are read by the chain's MMAs, issued after the barrier that ends R^T
             tc::fence_async_smem();
-            __syncthreads();
 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
             // every thread reads D2 and V^T only after its own wait, and this phase writes no
@@ -1154,9 +1154,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 pend_tok0 = tok0;
                 pend_n = n;
             }
-            tc::fence_before_sync();
-            __syncthreads();
-            tc::fence_after_sync();
+            // no barrier here: the staged tile is read (store_o) after the next chunk's first
+            // checked barrier, and nothing before that barrier writes what this epilogue reads
         }
         if (!sync_ok(err)) break;
         if (pend_n > 0) {  // the last chunk's output (staged before the barrier above)
