@@ -89,8 +89,8 @@ constexpr uint32_t SM_T00 = SM_P + 16384;        // tf32 SW128 [32 t][32 i]  (I 
 constexpr uint32_t SM_T11 = SM_T00 + 4096;       // tf32 SW128 [32 t][32 i]  (I + A11)^{-1}
 constexpr uint32_t SM_NA10 = SM_T11 + 4096;      // tf32 SW128 [32 t][32 i]  -A[32 + t][i]
 constexpr uint32_t SM_ID = SM_NA10 + 8192;       // bf16 SW128 [64][64] identity (1024-aligned)
-constexpr uint32_t AT_LD = 68;                   // padded row of the fp32 A^T tile
-constexpr uint32_t SM_AT = SM_ID + 8192;         // fp32 A^T [64 i][68]; later the bf16 O tile
+constexpr uint32_t AT_LD = 68;                   // 64 x AT_LD fp32: the space of the output tile
+constexpr uint32_t SM_AT = SM_ID + 8192;         // bf16 O tile [64 t][O_LD]
 constexpr uint32_t O_LD = 136;                   // padded row (bf16) of the output staging tile
 constexpr uint32_t SM_SMALL = SM_AT + 64 * AT_LD * 4;
 // small region (floats)
@@ -107,8 +107,14 @@ constexpr uint32_t SM_RAW = SM_KQG;             // bf16 [67 rows][384 channels]
 constexpr int RAW_ROWS = TC_C + 3;              // chunk + halo of the longest conv (4 taps)
 constexpr uint32_t RAW_LD = 3 * TC_D * 2;       // bytes per raw row
 static_assert(RAW_ROWS * RAW_LD <= 65536, "raw rows fit the K|Q staging buffer");
-constexpr uint32_t SM_BYTES = SM_CB + 3 * TC_D * 4;
+// the two 32 x 32 diagonal blocks of A, transposed (fp32 [2][32 i][AD_LD]), the triangular
+// solves' input: apart from the output tile, whose previous chunk's copy is still being stored
+constexpr uint32_t AD_LD = 36;
+constexpr uint32_t SM_AD = SM_CB + 3 * TC_D * 4;
+constexpr uint32_t SM_BYTES = SM_AD + 2 * 32 * AD_LD * 4;
 constexpr size_t TC_SMEM = SM_BYTES + 1024;                // alignment slack
+static_assert(TC_SMEM <= 227 * 1024, "the block's shared memory fits an SM");
+static_assert(TC_C * O_LD * 2 <= TC_C * AT_LD * 4, "the output tile fits its space");
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct TcParams {
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                           ~static_cast<uintptr_t>(1023));
     float *sf = reinterpret_cast<float *>(sm + SM_SMALL);
-    float *atp = reinterpret_cast<float *>(sm + SM_AT);
+    float *adp = reinterpret_cast<float *>(sm + SM_AD);
     uint64_t *bar_a = reinterpret_cast<uint64_t *>(sm + SM_BARS);
     uint64_t *bar_b = bar_a + 1;
     uint64_t *bar_c = reinterpret_cast<uint64_t *>(sm + SM_BARS + 40);  // state update done
@@ -868,7 +874,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 __syncthreads();
                 tc::fence_after_sync();
             }
-            if (!sync_ok(err)) break;
+            // no barrier: each thread reads D1 after its own wait, and the tiles written below
+            // (A's diagonal blocks, P, -A10) have no reader left from before
             if (KDA && !FRONT && !last) {  // KDA: K|Q tile consumed (the staging pass or the
                                            // exact D1): the next chunk's in flight
                 if (use_tma && !alt) tma_kq(kh, tok0 + TC_C, SM_KQ);
@@ -917,7 +924,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                                         tc::to_tf32_operand(v[q4 * 4 + 2]), tc::to_tf32_operand(v[q4 * 4 + 3]));
                 } else {
 #pragma unroll
-                    for (int ii = 0; ii < 16; ++ii) atp[(i0 + ii) * AT_LD + r] = v[ii];
+                    if ((i0 >> 5) == (r >> 5)) {  // a diagonal block: A00 or A11, transposed
+                        float *adb = adp + (r >> 5) * 32 * AD_LD;
+#pragma unroll
+                        for (int ii = 0; ii < 16; ++ii) adb[((i0 & 31) + ii) * AD_LD + (r & 31)] = v[ii];
+                    }
                     if (r >= 32 && i0 < 32) {  // -A10, the coupling of the two 32-token halves
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4)
@@ -942,17 +953,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 float x[8];
 #pragma unroll
                 for (int m = 0; m < 8; ++m) x[m] = (4 * m + p == jj) ? 1.f : 0.f;
-                const float *ab = atp + o * AT_LD + o + p;  // ab[i*AT_LD + 4m] = A[o+4m+p][o+i]
+                const float *ab = adp + b * 32 * AD_LD + p;  // ab[i*AD_LD + 4m] = A[o+4m+p][o+i]
 #pragma unroll
                 for (int i = 0; i < 31; ++i) {
                     const int m0 = i >> 2;
                     const float xi = __shfl_sync(0xffffffffu, x[m0], (lane & ~3) | (i & 3));
                     {
-                        const float nx = fmaf(-ab[i * AT_LD + 4 * m0], xi, x[m0]);
+                        const float nx = fmaf(-ab[i * AD_LD + 4 * m0], xi, x[m0]);
                         x[m0] = (p > (i & 3)) ? nx : x[m0];
                     }
 #pragma unroll
-                    for (int m = m0 + 1; m < 8; ++m) x[m] = fmaf(-ab[i * AT_LD + 4 * m], xi, x[m]);
+                    for (int m = m0 + 1; m < 8; ++m) x[m] = fmaf(-ab[i * AD_LD + 4 * m], xi, x[m]);
                 }
                 const uint32_t tile = b == 0 ? SM_T00 : SM_T11;
 #pragma unroll
