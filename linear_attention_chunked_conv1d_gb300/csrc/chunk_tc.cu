@@ -544,6 +544,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
             }
         }
+        // KDA: a chunk's cumulative gates in base-2 units, gc[C16*part + t][c] log2(e) (c = row),
+        // are formed in pre_gk one chunk ahead, in two halves around a barrier of the chunk
+        // before (the partial sums of the four row parts meet in shared memory); the chunk
+        // itself then starts from them without a barrier of its own. gates_sum: this thread's
+        // 16 rows; gates_carry: the earlier parts' totals, gc_L and e^{gc_L}, beta.
+        auto gates_sum = [&]() {
+            float acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < C16; ++t) {
+                acc = fmaf(pre_gk[t], LOG2E, acc);
+                pre_gk[t] = acc;
+            }
+            sf[SF_CARRY + part * 128 + row] = acc;
+        };
+        auto gates_carry = [&]() {
+            float carry = 0.f;
+#pragma unroll
+            for (int pp = 0; pp < NQ - 1; ++pp)
+                if (pp < part) carry += sf[SF_CARRY + pp * 128 + row];
+#pragma unroll
+            for (int t = 0; t < C16; ++t) pre_gk[t] += carry;
+            if (part == NQ - 1) {
+                sf[SF_GL + row] = pre_gk[C16 - 1];  // base 2
+                sf[SF_EL + row] = tc::ex2(pre_gk[C16 - 1]);
+            }
+            if (tid < TC_C) sf[SF_BETA + tid] = pre_b;
+        };
+        if (KDA) {  // the first chunk's
+            gates_sum();
+            __syncthreads();
+            gates_carry();
+        }
 
         // Global stores of a chunk's output tile, staged as bf16 [t][d] in the A^T buffer; they
         // are issued in the next chunk while its first MMAs run (or after the last chunk).
@@ -591,33 +623,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             const uint32_t kqo = (KDA || !(ch & 1)) ? SM_KQ : SM_KQ1;
             const uint32_t kqo_next = (KDA || (ch & 1)) ? SM_KQ : SM_KQ1;
 
-            // ---------------- gates
-            // KDA: the cumulative gates in base-2 units, gc[C16*part + t][c] log2(e) (c = row), so
-            // that every decay factor below is one ex2
+            // ---------------- gates (KDA: formed one chunk ahead; every decay factor below is one
+            //                  ex2 of them)
             float gcr[KDA ? C16 : 1];
             if (KDA) {
-                float acc = 0.f;
 #pragma unroll
-                for (int t = 0; t < C16; ++t) {
-                    acc = fmaf(pre_gk[t], LOG2E, acc);
-                    gcr[t] = acc;
-                }
-                sf[SF_CARRY + part * 128 + row] = acc;
+                for (int t = 0; t < C16; ++t) gcr[t] = pre_gk[t];
                 if (tid == 0) *slow_sh = 0;
             }
-            if (tid < TC_C) {
+            if (!KDA && tid < TC_C) {
                 const int t = tid;
                 sf[SF_BETA + t] = pre_b;
-                if (!KDA) {
-                    float x = pre_g;
+                float x = pre_g;
 #pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, x, off);
-                        if (lane >= off) x += y;
-                    }
-                    if (lane == 31) sf[SF_WARP + warp] = x;
-                    sf[SF_GC + t] = x;  // warp-local; carried below
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if (lane >= off) x += y;
                 }
+                if (lane == 31) sf[SF_WARP + warp] = x;
+                sf[SF_GC + t] = x;  // warp-local; carried below
             }
             cp_async_wait_all();
             if (use_tma) {  // this chunk's K|Q and V tiles (the K|Q may have been waited already)
@@ -632,21 +656,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 uint32_t never = 0;
                 wait_bar(bar_e, never);
             }
-            if (!sync_ok(err)) break;
+            if (!KDA && !sync_ok(err)) break;  // GDN: the scalar gates meet in shared memory
             // this chunk's scalar gates are in shared memory: fetch the next chunk's
             if (!last) fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
-            if (KDA) {
-                float carry = 0.f;
-#pragma unroll
-                for (int pp = 0; pp < NQ - 1; ++pp)
-                    if (pp < part) carry += sf[SF_CARRY + pp * 128 + row];
-#pragma unroll
-                for (int t = 0; t < C16; ++t) gcr[t] += carry;
-                if (part == NQ - 1) {
-                    sf[SF_GL + row] = gcr[C16 - 1];  // base 2
-                    sf[SF_EL + row] = tc::ex2(gcr[C16 - 1]);
-                }
-            } else if (tid < TC_C) {
+            if (!KDA && tid < TC_C) {
                 const float gct = sf[SF_GC + tid] + (tid >= 32 ? sf[SF_WARP] : 0.f);
                 sf[SF_GC + tid] = gct;
                 sf[SF_GC2 + tid] = gct * LOG2E;
@@ -668,7 +681,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 }
                 tc::fence_async_smem();
             }
-            __syncthreads();
+            if (KDA) {
+                if (!sync_ok(err)) break;  // KDA's first barrier of the chunk
+            } else {
+                __syncthreads();
+            }
             if (!KDA && tid < TC_C) {
                 const float gct = sf[SF_GC + tid], gL = sf[SF_GC + TC_C - 1];
                 const float gm = sf[SF_GC + TC_C / 2 - 1];
@@ -1069,6 +1086,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 }
                 tc::tmem_wait_st();
             }
+            if (KDA && !last) gates_sum();  // the next chunk's (its loads issued during D1)
             wait_bar(bar_b, phase_b);  // each thread reads the chain's results after its own wait
 
             // ------ U'^T -> TMEM (tf32); GDN also Ud^T = U'^T diag(e^{gc_L - gc}) for the state
@@ -1138,6 +1156,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::mma_commit(bar_c);
             }
             pend_c = true;
+            // the next chunk's gates, second half: this chunk's beta, gc_L and e^{gc_L} were last
+            // read before the barrier above
+            if (KDA && !last) gates_carry();
             if (FRONT && !last) {  // next chunk's q, k, v tiles while the tensor core works
                 conv_tile_any(a, sm, min(TC_C, len - (ch + 1) * TC_C), pad_qk, warp, lane, kqo_next);
                 tc::fence_async_smem();
