@@ -957,7 +957,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             }
             tc::fence_async_smem();
             tc::fence_before_sync();
-            __syncthreads();
+            // Each reader waits for its own writers only (hardware barriers 1-3): A00 is written by
+            // warps 0 and 4 and solved by warps 8-11; A11 is written by warps 9 and 13 and solved
+            // by warps 12-15; warp 0 issues D2 once every warp has read D1 (GDN's V^T lands in
+            // D1's columns). P and -A10 are read by MMAs issued after the barrier that ends R^T.
+            if (warp == 0 || warp == 4) named_arrive(1, 6 * 32);
+            if (warp == 9) named_arrive(2, 5 * 32);
+            if (warp != 0) named_arrive(3, TC_THREADS);
 
             // ---------------- T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} (the two 32-token
             //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores by
@@ -966,6 +972,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             //   U'0 = R0 T00^T, U'1 = (R1 - U'0 A10^T) T11^T.
             if (warp >= 8) {
                 const int w8 = warp - 8, b = w8 >> 2, o = 32 * b;
+                named_sync(1 + b, b == 0 ? 6 * 32 : 5 * 32);  // this block of A is written
                 const int jj = 8 * (w8 & 3) + (lane >> 2), p = lane & 3;
                 float x[8];
 #pragma unroll
@@ -986,8 +993,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
                     st_tf32(sm, tile + tc::sw128_offset(4 * m + p, jj, 32, 4), x[m]);
-            } else {
-                if (warp == 0) issue_mma2();
+            } else if (warp == 0) {
+                named_sync(3, TC_THREADS);  // every warp has read D1
+                issue_mma2();
             }
             // the T blocks are read by the chain's MMAs, issued after the barrier that ends R^T
             tc::fence_async_smem();

@@ -41,6 +41,11 @@ __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Arrival on hardware barrier `id` without waiting (the threads that sync on it see this
+// thread's earlier shared-memory writes once it completes).
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // One arrival on an mbarrier (release at CTA scope: the caller's earlier shared-memory writes
 // are visible to a thread whose wait on this phase succeeds).
