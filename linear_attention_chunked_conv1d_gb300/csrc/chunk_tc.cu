@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
     const bool use_tma = !FRONT && P.tma != 0;
     uint32_t par_kq = 0, par_v = 0;
     bool fly_kq = false, fly_v = false;
-    auto tma_kq = [&](int kh_, int tok, uint32_t kqo) {
-        if (tid == 0) {
+    auto tma_kq = [&](int kh_, int tok, uint32_t kqo, int issuer = 0) {
+        if (tid == issuer) {
             tc::fence_async_smem();  // earlier generic accesses of the tile come first
             tc::mbar_expect_tx(bar_kq, 32768u);
             const int x = kh_ * TC_D;
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tma_wait(bar_v, par_v);
                 par_kq ^= 1u;
                 par_v ^= 1u;
-                if (tid == 0) fly_kq = fly_v = false;
+                fly_kq = fly_v = false;
             }
             tc::fence_async_smem();
             if (a.debug_stall) {  // test knob: a wait on a barrier nothing completes runs out
@@ -893,10 +893,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             }
             // no barrier: each thread reads D1 after its own wait, and the tiles written below
             // (A's diagonal blocks, P, -A10) have no reader left from before
-            if (KDA && !FRONT && !last) {  // KDA: K|Q tile consumed (the staging pass or the
-                                           // exact D1): the next chunk's in flight
-                if (use_tma && !alt) tma_kq(kh, tok0 + TC_C, SM_KQ);
-                else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
+            // KDA: K|Q tile consumed (the staging pass or the exact D1): the next chunk's in
+            // flight (a TMA tile is issued after the A/P pass, below)
+            if (KDA && !FRONT && !last && !(use_tma && !alt)) {
+                load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid);
                 cp_async_commit();
             }
 
@@ -964,6 +964,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             if (warp == 0 || warp == 4) named_arrive(1, 6 * 32);
             if (warp == 9) named_arrive(2, 5 * 32);
             if (warp != 0) named_arrive(3, TC_THREADS);
+            // KDA's next K|Q tile by TMA, from warp 7: it has no share in the solves and waits
+            // for D2 next, while warp 0 (an A00 writer) goes straight on to D2's issue
+            if (KDA && !FRONT && !last && use_tma && !alt) tma_kq(kh, tok0 + TC_C, SM_KQ, 7 * 32);
 
             // ---------------- T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} (the two 32-token
             //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores by
@@ -1028,7 +1031,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::tmem_wait_st();
             }
             tc::fence_before_sync();
-            __syncthreads();
+            // The chain's first product reads R0^T (written by warps 0-7) and T00 (warps 8-11),
+            // its second and third R1^T (warps 8-15) and T11 (warps 12-15): warp 0 waits for
+            // each group on its own hardware barrier (4, then 5). The other warps go on to the
+            // state decay below, which touches nothing the chain reads: GDN's at once, KDA's
+            // once warps 1-15 have all arrived (barrier 6; its decay and gate sums, started
+            // early, take issue slots from the warps the chain waits for).
+            if (warp >= 1 && warp < 12) named_arrive(4, 12 * 32);
+            if (warp >= 8) named_arrive(5, 9 * 32);
+            if (KDA && warp >= 1) named_sync(6, 15 * 32);
 
             // ---------------- block substitution, one thread: U'0^T = R0^T T00^T;
             //   Z^T = R1^T - U'0^T A10^T (accumulated onto R1^T); U'1^T = Z^T T11^T (into the
@@ -1036,16 +1047,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             //   A operand straight from TMEM, without the rounding step; MMAs into
             //   different accumulators are not ordered, so the issuing thread waits on bar_d
             //   (two completions per chunk: parities 0, then 1) between them.
-            if (warp == 0 && tc::elect_one()) {
+            constexpr uint32_t id32 = tc::idesc(128, 32, tc::FMT_TF32);
+            auto issue_t00 = [&]() {  // U'0^T = R0^T T00^T
                 tc::fence_after_sync();
-                constexpr uint32_t id32 = tc::idesc(128, 32, tc::FMT_TF32);
-                bool ok = true;
 #pragma unroll
                 for (uint32_t kk = 0; kk < 4; ++kk)
                     tc::mma_tf32_ts(tm + COL_D6, tm + COL_RU + kk * 8,
                                     tc::sdesc_sw128((sb + SM_T00) + kk * 32u), id32, kk > 0);
                 tc::mma_commit(bar_d);
-                ok = tc::mbar_wait(bar_d, 0, wait_ns);
+            };
+            if (warp == 0) {
+                named_sync(4, 12 * 32);
+                if (tc::elect_one()) issue_t00();
+                __syncwarp();
+                named_sync(5, 9 * 32);
+            }
+            if (warp == 0 && tc::elect_one()) {
+                tc::fence_after_sync();
+                bool ok = tc::mbar_wait(bar_d, 0, wait_ns);
                 tc::fence_after_sync();
                 if (ok) {
 #pragma unroll
@@ -1221,8 +1240,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 
     cp_async_wait_all();
     // a TMA load still in flight after an error lands before the block exits
-    if (tid == 0 && fly_kq) tc::mbar_wait(bar_kq, par_kq, WAIT_NS);
-    if (tid == 0 && fly_v) tc::mbar_wait(bar_v, par_v, WAIT_NS);
+    if (fly_kq) tc::mbar_wait(bar_kq, par_kq, WAIT_NS);  // by the thread that issued it
+    if (fly_v) tc::mbar_wait(bar_v, par_v, WAIT_NS);
     // Every MMA of this block has completed before its TMEM is released, also after a wait gave
     // up: the issuing lane commits once more (a commit tracks all earlier MMAs of its thread)
     // and waits for that commit with the full limit.
