@@ -420,10 +420,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
         }
     };
 
-    // TMA loads of the K|Q and V tiles (plain calls): thread 0 issues the boxes of a chunk, one
+    // TMA loads of the K|Q and V tiles (plain calls): one thread issues the boxes of a chunk, one
     // load per tile and chunk in flight at most; every thread waits for a tile's phase before
-    // its first use (par_*: parity of the next load to be consumed; fly_*: thread 0's record of
-    // an issued load that has not been consumed, drained on exit)
+    // its first use (par_*: parity of the next load to be consumed; fly_*: the issuing thread's
+    // record of a load that has not been consumed, drained on exit)
     const bool use_tma = !FRONT && P.tma != 0;
     uint32_t par_kq = 0, par_v = 0;
     bool fly_kq = false, fly_v = false;
@@ -578,12 +578,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
         }
 
         // Global stores of a chunk's output tile, staged as bf16 [t][d] in the A^T buffer; they
-        // are issued in the next chunk while its first MMAs run (or after the last chunk).
-        auto store_o = [&](int tok0s, int ns) {
+        // are issued in the next chunk while its first MMAs run (or after the last chunk). Within
+        // the chunk loop of the recurrence-only launch warp 0 has no share: it issues D1 then and
+        // writes part of A00 next.
+        auto store_o = [&](int tok0s, int ns, bool all) {
             const __nv_bfloat16 *os = reinterpret_cast<const __nv_bfloat16 *>(sm + SM_AT);
-#pragma unroll
-            for (int m = 0; m < 1024 / TC_THREADS; ++m) {
-                const int idx = tid + TC_THREADS * m;  // 0..1023
+            auto store_piece = [&](int idx) {  // row idx / 16, channels 8 (idx % 16) ..
                 const int t = idx >> 4, cj = idx & 15;
                 __nv_bfloat16 *dst = og + (int64_t)(tok0s + t) * Hv * TC_D + cj * 8;
                 if (a.z) {
@@ -609,6 +609,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 } else if (t < ns) {
                     *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
                 }
+            };
+            if (all) {
+#pragma unroll
+                for (int m = 0; m < 1024 / TC_THREADS; ++m) store_piece(tid + TC_THREADS * m);
+            } else if (warp != 0) {  // 480 threads: a warp's 16-lane groups stay aligned
+                for (int idx = tid - 32; idx < 1024; idx += TC_THREADS - 32) store_piece(idx);
             }
         };
         int pend_tok0 = 0, pend_n = 0;  // output tile staged, not yet stored
@@ -806,9 +812,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 // the previous state update is complete: S may be read, and the K|Q buffer it
                 // read takes the next chunk's tile
                 wait_state();
-                if (!FRONT && !last) {
-                    if (use_tma && !alt) tma_kq(kh, tok0 + TC_C, kqo_next);
-                    else load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid, kqo_next);
+                if (!FRONT && !last && !(use_tma && !alt)) {  // (a TMA tile: after the A/P pass)
+                    load_kq(a, sm, tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C), kh, tid, kqo_next);
                     cp_async_commit();
                 }
                 // S -> S_hi = bf16(S), S_lo = bf16(S - S_hi), packed two per column, D2's A
@@ -854,7 +859,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 }
             }
             if (pend_n > 0) {  // previous chunk's output while D1 is computed
-                store_o(pend_tok0, pend_n);
+                store_o(pend_tok0, pend_n, FRONT);
                 pend_n = 0;
             }
 
@@ -964,9 +969,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             if (warp == 0 || warp == 4) named_arrive(1, 6 * 32);
             if (warp == 9) named_arrive(2, 5 * 32);
             if (warp != 0) named_arrive(3, TC_THREADS);
-            // KDA's next K|Q tile by TMA, from warp 7: it has no share in the solves and waits
-            // for D2 next, while warp 0 (an A00 writer) goes straight on to D2's issue
-            if (KDA && !FRONT && !last && use_tma && !alt) tma_kq(kh, tok0 + TC_C, SM_KQ, 7 * 32);
+            // The next K|Q tile by TMA, from warp 7: it has no share in the solves and waits for
+            // D2 next, while warp 0 (an A00 writer) goes straight on to D2's issue
+            if (!FRONT && !last && use_tma && !alt) tma_kq(kh, tok0 + TC_C, kqo_next, 7 * 32);
 
             // ---------------- T00 = (I + A00)^{-1}, T11 = (I + A11)^{-1} (the two 32-token
             //   diagonal blocks of (I + A)^{-1}), fp32 forward substitution on CUDA cores by
@@ -1218,7 +1223,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
         }
         if (!sync_ok(err)) break;
         if (pend_n > 0) {  // the last chunk's output (staged before the barrier above)
-            store_o(pend_tok0, pend_n);
+            store_o(pend_tok0, pend_n, true);
             pend_n = 0;
         }
 
