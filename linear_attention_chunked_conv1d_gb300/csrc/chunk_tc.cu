@@ -960,12 +960,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     }
                 }
             }
-            tc::fence_async_smem();
             tc::fence_before_sync();
             // Each reader waits for its own writers only (hardware barriers 1-3): A00 is written by
             // warps 0 and 4 and solved by warps 8-11; A11 is written by warps 9 and 13 and solved
             // by warps 12-15; warp 0 issues D2 once every warp has read D1 (GDN's V^T lands in
-            // D1's columns). P and -A10 are read by MMAs issued after the barrier that ends R^T.
+            // D1's columns). P and -A10 are read by MMAs issued after the barriers that end R^T
+            // (their proxy fence is there, when these stores have long drained).
             if (warp == 0 || warp == 4) named_arrive(1, 6 * 32);
             if (warp == 9) named_arrive(2, 5 * 32);
             if (warp != 0) named_arrive(3, TC_THREADS);
@@ -1005,8 +1005,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 named_sync(3, TC_THREADS);  // every warp has read D1
                 issue_mma2();
             }
-            // the T blocks are read by the chain's MMAs, issued after the barrier that ends R^T
-            tc::fence_async_smem();
+            // the T blocks are read by the chain's MMAs, issued after the barriers that end R^T
+            // (the proxy fence before them covers these stores)
 
             // ------ D2, V^T ready: R^T = beta (V^T - e^gc D2[:, :64]) -> TMEM
             // every thread reads D2 and V^T only after its own wait, and this phase writes no
@@ -1035,6 +1035,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 if (t0c >= 32) tc::tmem_st16(tc::tmem_addr(tm, lq, COL_D6 + t0c), v);  // Z = R1
                 tc::tmem_wait_st();
             }
+            tc::fence_async_smem();  // P, -A10 and the T blocks, for the MMAs after these barriers
             tc::fence_before_sync();
             // The chain's first product reads R0^T (written by warps 0-7) and T00 (warps 8-11),
             // its second and third R1^T (warps 8-15) and T11 (warps 12-15): warp 0 waits for
