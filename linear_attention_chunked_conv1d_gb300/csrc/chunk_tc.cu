@@ -666,9 +666,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             // this chunk's scalar gates are in shared memory: fetch the next chunk's
             if (!last) fetch_gates(tok0 + TC_C, min(TC_C, len - (ch + 1) * TC_C));
             if (!KDA && tid < TC_C) {
-                const float gct = sf[SF_GC + tid] + (tid >= 32 ? sf[SF_WARP] : 0.f);
+                // gc_t, and the chunk's decay factors from it: gc at rows 31 and 63 are the two
+                // warps' totals (so no barrier is needed before the factors)
+                const float w0t = sf[SF_WARP];
+                const float gct = sf[SF_GC + tid] + (tid >= 32 ? w0t : 0.f);
+                const float gL = w0t + sf[SF_WARP + 1], gm = w0t;
                 sf[SF_GC + tid] = gct;
                 sf[SF_GC2 + tid] = gct * LOG2E;
+                sf[SF_EG + tid] = __expf(gct);
+                sf[SF_EGL + tid] = __expf(gL - gct);
+                // e^{gc_t - gc_i} = e^{gc_t - gc_m} e^{gc_m - gc_i} (m = row 31): both factors
+                // are bounded by the half-chunk decay range, checked below
+                sf[SF_RF + tid] = __expf(gct - gm);
+                sf[SF_CF + tid] = __expf(gm - gct);
             }
             // Pad rows of the K|Q tile carry pad_fill; every consumer removes them by select.
             // The V tile's pad rows are zero: it is contracted over tokens by the transposing
@@ -687,21 +697,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 }
                 tc::fence_async_smem();
             }
-            if (KDA) {
-                if (!sync_ok(err)) break;  // KDA's first barrier of the chunk
-            } else {
-                __syncthreads();
-            }
-            if (!KDA && tid < TC_C) {
-                const float gct = sf[SF_GC + tid], gL = sf[SF_GC + TC_C - 1];
-                const float gm = sf[SF_GC + TC_C / 2 - 1];
-                sf[SF_EG + tid] = __expf(gct);
-                sf[SF_EGL + tid] = __expf(gL - gct);
-                // e^{gc_t - gc_i} = e^{gc_t - gc_m} e^{gc_m - gc_i} (m = row 31): both factors
-                // are bounded by the half-chunk decay range, checked below
-                sf[SF_RF + tid] = __expf(gct - gm);
-                sf[SF_CF + tid] = __expf(gm - gct);
-            }
+            if (KDA && !sync_ok(err)) break;  // KDA's first barrier of the chunk (GDN: the
+                                              // barrier before D1 follows)
 
             // ---------------- D1 = [K;Q] K^T (KDA: tf32, decays split per factor)
             bool slow = false;
