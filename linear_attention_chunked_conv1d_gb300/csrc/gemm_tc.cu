@@ -37,6 +37,7 @@ constexpr size_t G_SMEM = G_BAR + 256 + 1024;     // + barriers + alignment slac
 constexpr int G_THREADS = 192;
 constexpr uint32_t ACC_COLS = 2 * GN;             // two accumulators
 constexpr uint64_t G_WAIT_NS = 2000000000ull;
+constexpr uint32_t G_SLEEP_NS = 1000000u;  // a waiting thread sleeps up to 1 ms between tests
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
@@ -91,7 +92,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 const int m0 = (tile / nt) * GM, n0 = (tile % nt) * GN;
                 for (int k = 0; k < kb; ++k, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!tc::mbar_wait(empty + s, ph ^ 1u, wait_ns) || *err) {
+                    if (!tc::mbar_wait(empty + s, ph ^ 1u, wait_ns, G_SLEEP_NS) || *err) {
                         *err = 1;
                         break;
                     }
@@ -104,7 +105,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             // one on stage s was copy number it - 1 - ((it - 1 - s) mod STAGES)
             for (uint32_t s = 0; s < STAGES && s < it; ++s) {
                 const uint32_t last = it - 1 - ((it - 1 - s) % STAGES);
-                if (!tc::mbar_wait(full + s, (last / STAGES) & 1u, G_WAIT_NS)) *err = 1;
+                if (!tc::mbar_wait(full + s, (last / STAGES) & 1u, G_WAIT_NS, G_SLEEP_NS)) *err = 1;
             }
         }
     } else if (warp == 1) {
@@ -113,10 +114,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             uint32_t it = 0, tcnt = 0;
             // test knob: a wait on a barrier nothing has completed yet (its first phase ends
             // with the final commit below) runs out, and the block unwinds
-            if (debug_stall && !tc::mbar_wait(fin, 0, wait_ns)) *err = 1;
+            if (debug_stall && !tc::mbar_wait(fin, 0, wait_ns, G_SLEEP_NS)) *err = 1;
             for (int tile = blockIdx.x; tile < ntiles && !*err; tile += gridDim.x, ++tcnt) {
                 const uint32_t acc = tcnt & 1u, aph = (tcnt >> 1) & 1u;
-                if (!tc::mbar_wait(acce + acc, aph ^ 1u, wait_ns)) {
+                if (!tc::mbar_wait(acce + acc, aph ^ 1u, wait_ns, G_SLEEP_NS)) {
                     *err = 1;
                     break;
                 }
@@ -125,7 +126,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 bool ok = true;
                 for (int k = 0; k < kb; ++k, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!tc::mbar_wait(full + s, ph, wait_ns) || *err) {
+                    if (!tc::mbar_wait(full + s, ph, wait_ns, G_SLEEP_NS) || *err) {
                         ok = false;
                         break;
                     }
@@ -145,7 +146,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             }
             // every MMA this thread issued must have completed before the block exits
             tc::mma_commit(fin);
-            if (!tc::mbar_wait(fin, 0, G_WAIT_NS)) *err = 1;
+            if (!tc::mbar_wait(fin, 0, G_WAIT_NS, G_SLEEP_NS)) *err = 1;
         }
     } else {  // ---- epilogue: warps 2-5, TMEM lane quadrant warp % 4
         const uint32_t q = warp & 3;
@@ -154,7 +155,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             // every decision to stop is made per warp: the TMEM loads below are warp-collective
             if (__any_sync(0xffffffffu, *err != 0)) break;
             const uint32_t acc = tcnt & 1u, aph = (tcnt >> 1) & 1u;
-            if (!__all_sync(0xffffffffu, tc::mbar_wait(accf + acc, aph, wait_ns))) {
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(accf + acc, aph, wait_ns, G_SLEEP_NS))) {
                 *err = 1;
                 break;
             }

@@ -224,14 +224,33 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// The same test with a suspend-time hint: a thread whose phase is not complete sleeps until it
+// completes or `hint_ns` nanoseconds have passed, instead of returning at once (waiting threads
+// then take no issue slots from the others).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Waits for phase `parity` of `bar` to complete, giving up after `limit_ns` nanoseconds.
-// Returns false on timeout (the caller records an error and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+// Returns false on timeout (the caller records an error and unwinds). With `sleep_ns` > 0 the
+// waiting thread sleeps between tests (for threads that wait long while others work: the
+// GEMM's epilogue warps during a tile's main loop); without, it polls (the recurrence's waits,
+// which are short and on its critical path: there the sleep form was slower).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                          uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+        if (sleep_ns ? mbar_try_wait_sleep(bar, parity, sleep_ns) : mbar_try_wait(bar, parity))
+            return true;
+        if ((i & (sleep_ns ? 3u : 63u)) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
