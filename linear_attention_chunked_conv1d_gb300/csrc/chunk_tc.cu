@@ -578,10 +578,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
         }
 
         // Global stores of a chunk's output tile, staged as bf16 [t][d] in the A^T buffer; they
-        // are issued in the next chunk while its first MMAs run (or after the last chunk). Within
-        // the chunk loop of the recurrence-only launch warp 0 has no share: it issues D1 then and
-        // writes part of A00 next.
-        auto store_o = [&](int tok0s, int ns, bool all) {
+        // are issued in the next chunk (or after the last chunk) by warps w0 .. w0 + nw - 1.
+        // Within the chunk loop: in GDN's recurrence-only launch by warps 1-7 while warps 8-15
+        // solve and warp 0 issues D2 (their wait for D2 has nothing else to overlap); in KDA's
+        // by warps 1-15 while D1 runs (warp 0 issues it and writes part of A00 next; there the
+        // later placement was slower); in the fused launch by all warps while D1 runs.
+        auto store_o = [&](int tok0s, int ns, int w0, int nw) {
             const __nv_bfloat16 *os = reinterpret_cast<const __nv_bfloat16 *>(sm + SM_AT);
             auto store_piece = [&](int idx) {  // row idx / 16, channels 8 (idx % 16) ..
                 const int t = idx >> 4, cj = idx & 15;
@@ -610,11 +612,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
                 }
             };
-            if (all) {
+            if (nw == TC_THREADS / 32) {
 #pragma unroll
                 for (int m = 0; m < 1024 / TC_THREADS; ++m) store_piece(tid + TC_THREADS * m);
-            } else if (warp != 0) {  // 480 threads: a warp's 16-lane groups stay aligned
-                for (int idx = tid - 32; idx < 1024; idx += TC_THREADS - 32) store_piece(idx);
+            } else if (warp >= w0 && warp < w0 + nw) {  // whole warps: 16-lane groups aligned
+                for (int idx = tid - 32 * w0; idx < 1024; idx += 32 * nw) store_piece(idx);
             }
         };
         int pend_tok0 = 0, pend_n = 0;  // output tile staged, not yet stored
@@ -855,8 +857,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                     pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
                 }
             }
-            if (pend_n > 0) {  // previous chunk's output while D1 is computed
-                store_o(pend_tok0, pend_n, FRONT);
+            if ((FRONT || KDA) && pend_n > 0) {  // previous chunk's output while D1 is computed
+                store_o(pend_tok0, pend_n, FRONT ? 0 : 1, FRONT ? TC_THREADS / 32 : TC_THREADS / 32 - 1);
                 pend_n = 0;
             }
 
@@ -1001,7 +1003,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             } else if (warp == 0) {
                 named_sync(3, TC_THREADS);  // every warp has read D1
                 issue_mma2();
+            } else if (!FRONT && !KDA && pend_n > 0) {  // previous chunk's output (warps 1-7)
+                store_o(pend_tok0, pend_n, 1, 7);
             }
+            if (!FRONT && !KDA) pend_n = 0;
             // the T blocks are read by the chain's MMAs, issued after the barriers that end R^T
             // (the proxy fence before them covers these stores)
 
@@ -1221,7 +1226,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
         }
         if (!sync_ok(err)) break;
         if (pend_n > 0) {  // the last chunk's output (staged before the barrier above)
-            store_o(pend_tok0, pend_n, true);
+            store_o(pend_tok0, pend_n, 0, TC_THREADS / 32);
             pend_n = 0;
         }
 
