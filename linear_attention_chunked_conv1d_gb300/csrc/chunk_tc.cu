@@ -944,7 +944,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                             make_float4(tc::to_tf32_operand(v[q4 * 4]), tc::to_tf32_operand(v[q4 * 4 + 1]),
                                         tc::to_tf32_operand(v[q4 * 4 + 2]), tc::to_tf32_operand(v[q4 * 4 + 3]));
                 } else {
-#pragma unroll
                     if ((i0 >> 5) == (r >> 5)) {  // a diagonal block: A00 or A11, transposed
                         float *adb = adp + (r >> 5) * 32 * AD_LD;
 #pragma unroll
@@ -978,13 +977,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             //   coupling block is applied by the tensor core as a block substitution:
             //   U'0 = R0 T00^T, U'1 = (R1 - U'0 A10^T) T11^T.
             if (warp >= 8) {
-                const int w8 = warp - 8, b = w8 >> 2, o = 32 * b;
+                const int w8 = warp - 8, b = w8 >> 2;
                 named_sync(1 + b, b == 0 ? 6 * 32 : 5 * 32);  // this block of A is written
                 const int jj = 8 * (w8 & 3) + (lane >> 2), p = lane & 3;
                 float x[8];
 #pragma unroll
                 for (int m = 0; m < 8; ++m) x[m] = (4 * m + p == jj) ? 1.f : 0.f;
-                const float *ab = adp + b * 32 * AD_LD + p;  // ab[i*AD_LD + 4m] = A[o+4m+p][o+i]
+                const float *ab = adp + b * 32 * AD_LD + p;  // ab[i*AD_LD + 4m] = A[32b+4m+p][32b+i]
 #pragma unroll
                 for (int i = 0; i < 31; ++i) {
                     const int m0 = i >> 2;
