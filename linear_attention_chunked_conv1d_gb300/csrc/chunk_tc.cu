@@ -1093,10 +1093,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                 tc::mma_commit(bar_b);
             }
             // S <- S diag(e^{gc_L}) while the tensor core works (the chain above reads none of
-            // the state columns; the state MMA is issued after the barriers below). KDA: warp 0
-            // runs the chain, so warps 4 and 8 (the same TMEM lane quadrant) take its 32
-            // columns. (GDN keeps them on warp 0: there warps 1-15 also stage the next tile.)
-            if (!(KDA && warp == 0)) {
+            // the state columns; the state MMA is issued after the barriers below). Warp 0 runs
+            // the chain, so warps 4 and 8 (the same TMEM lane quadrant) take its 32 columns.
+            if (warp != 0) {
                 const int c0 = D32 * part;
                 float sv[D32];
 #pragma unroll
@@ -1109,13 +1108,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 #pragma unroll
                 for (int g = 0; g < D32 / 16; ++g)
                     tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + c0 + 16 * g), sv + 16 * g);
-                if (KDA && (warp == 4 || warp == 8)) {  // warp 0's columns, 16 each
+                if (warp == 4 || warp == 8) {  // warp 0's columns, 16 each
                     const int cs = warp == 4 ? 0 : 16;
                     float sx[16];
                     tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_S + cs), sx);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int ii = 0; ii < 16; ++ii) sx[ii] *= sf[SF_EL + cs + ii];
+                    for (int ii = 0; ii < 16; ++ii) sx[ii] *= KDA ? sf[SF_EL + cs + ii] : egL;
                     tc::tmem_st16(tc::tmem_addr(tm, lq, COL_S + cs), sx);
                 }
                 tc::tmem_wait_st();
