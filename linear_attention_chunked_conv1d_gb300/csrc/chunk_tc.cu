@@ -1199,23 +1199,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             wait_bar(bar_b, phase_b);  // each thread reads D4 after its own wait
 
             // ---------------- o = scale (e^gc (Q H) + P U'): staged as bf16 [t][d] in shared
-            //                  memory; written with 16-byte stores (rows < n) in the next chunk
+            //                  memory; written with 16-byte stores (rows < n) in the next chunk.
+            //                  GDN's recurrence-only launch: warp 0, held while the tensor core
+            //                  takes the state update, hands its 16 tokens to warp 12 (the same
+            //                  TMEM lane quadrant).
             {
                 __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + SM_AT);
-                const int t0c = C16 * part;
-                float vq[16], vp[16];
-                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
-                tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
-                tc::tmem_wait_ld();
+                auto epi = [&](const int t0c) {
+                    float vq[16], vp[16];
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
+                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                for (int ii = 0; ii < 16; ii += 2) {
-                    const int t = t0c + ii;
-                    const float o0 = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
-                    const float o1 = KDA ? vq[ii + 1] + vp[ii + 1] : fmaf(sf[SF_EG + t + 1], vq[ii + 1], vp[ii + 1]);
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(scale * o0, scale * o1);
-                    os[t * O_LD + row] = pr.x;
-                    os[(t + 1) * O_LD + row] = pr.y;
-                }
+                    for (int ii = 0; ii < 16; ii += 2) {
+                        const int t = t0c + ii;
+                        const float o0 = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
+                        const float o1 = KDA ? vq[ii + 1] + vp[ii + 1] : fmaf(sf[SF_EG + t + 1], vq[ii + 1], vp[ii + 1]);
+                        const __nv_bfloat162 pr = __floats2bfloat162_rn(scale * o0, scale * o1);
+                        os[t * O_LD + row] = pr.x;
+                        os[(t + 1) * O_LD + row] = pr.y;
+                    }
+                };
+                if (KDA || FRONT || warp != 0) epi(C16 * part);
+                if (!KDA && !FRONT && warp == 12) epi(0);
                 pend_tok0 = tok0;
                 pend_n = n;
             }
