@@ -1200,7 +1200,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 
             // ---------------- o = scale (e^gc (Q H) + P U'): staged as bf16 [t][d] in shared
             //                  memory; written with 16-byte stores (rows < n) in the next chunk.
-            //                  GDN's recurrence-only launch: warp 0, held while the tensor core
+            //                  In the recurrence-only launch warp 0, held while the tensor core
             //                  takes the state update, hands its 16 tokens to warp 12 (the same
             //                  TMEM lane quadrant).
             {
@@ -1220,8 +1220,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                         os[(t + 1) * O_LD + row] = pr.y;
                     }
                 };
-                if (KDA || FRONT || warp != 0) epi(C16 * part);
-                if (!KDA && !FRONT && warp == 12) epi(0);
+                if (FRONT || warp != 0) epi(C16 * part);
+                if (!FRONT && warp == 12) epi(0);
                 pend_tok0 = tok0;
                 pend_n = n;
             }
