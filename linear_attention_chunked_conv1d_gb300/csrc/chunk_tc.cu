@@ -331,6 +331,14 @@ __device__ __forceinline__ void write_conv_state(const RecArgs &a, const unsigne
     }
 }
 
+// A gate value read once: through the non-coherent path without allocating in L1 (the block's
+// shared memory leaves L1 little room, and the tile is not read again).
+__device__ __forceinline__ float ld_gate(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
 // Block-wide barrier that also reports whether any thread raised the local error flag. All
 // threads take the same branch: the flag is raised only by a wait that has run out, i.e. at
 // least the wait limit (1 ms or more) after that thread left this barrier, long after every
@@ -609,7 +617,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                         Vec16<__nv_bfloat16>::store(dst, ov);
                     }
                 } else if (t < ns) {
-                    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
+                    const uint4 ov = *reinterpret_cast<const uint4 *>(os + t * O_LD + cj * 8);
+                    if (FRONT) *reinterpret_cast<uint4 *>(dst) = ov;
+                    else __stcs(reinterpret_cast<uint4 *>(dst), ov);  // streamed: not read again here
                 }
             };
             if (nw == TC_THREADS / 32) {
@@ -854,7 +864,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
 #pragma unroll
                 for (int t = 0; t < C16; ++t) {
                     const int tt = C16 * part + t;
-                    pre_gk[t] = tt < nn ? gp[(int64_t)tt * Hv * TC_D] : 0.f;
+                    pre_gk[t] = tt < nn ? ld_gate(gp + (int64_t)tt * Hv * TC_D) : 0.f;
                 }
             }
             if ((FRONT || KDA) && pend_n > 0) {  // previous chunk's output while D1 is computed
