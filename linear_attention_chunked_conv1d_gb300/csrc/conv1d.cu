@@ -7,8 +7,9 @@
 // tokens of a batched prefill, advancing that request's conv state).
 //
 // GB300 design: the op is HBM-bound elementwise work, so each thread owns 4 channels (an 8-byte
-// bf16 / 16-byte fp32 vector) and a run of up to ROWS consecutive tokens of ONE stream,
-// keeping the kernel-1 previous rows in registers as a sliding window: x is read once (plus
+// bf16 / 16-byte fp32 vector) and a run of up to ROWS (64, 128 or 256: conv_rows) consecutive
+// tokens of ONE stream, keeping the kernel-1 previous rows in registers as a sliding window:
+// x is read once (plus
 // kernel-1 halo rows per run, served by L2) and out written once, with coalesced 16-byte
 // accesses. Runs are aligned to stream starts (stream s owns run slots floor(cu[s]/ROWS) + s
 // onwards, found by binary search), so the first run of a stream is the only one that reads
@@ -20,12 +21,12 @@
 namespace la {
 
 constexpr int CONV_THREADS = 128;
-constexpr int CONV_ROWS = 64;
+constexpr int CONV_ROWS = 64;  // the shortest run; a launch takes 64, 128 or 256 (conv_rows)
 constexpr int CONV_G_BF16 = 8;  // bf16 rows in flight per thread
 
-// First run slot of stream s.
-__device__ __forceinline__ int conv_run_base(const int32_t *cu, int s) {
-    return cu[s] / CONV_ROWS + s;
+// First run slot of stream s (runs of `rows` tokens).
+__device__ __forceinline__ int conv_run_base(const int32_t *cu, int s, int rows) {
+    return cu[s] / rows + s;
 }
 
 // One output row of a thread's 4 channels: y = SiLU(b + sum_m w_m xh_m) over the K-1 window
@@ -91,7 +92,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
                    const T *__restrict__ x, const T *__restrict__ w,
                    const T *__restrict__ bias, T *__restrict__ out,
                    const int32_t *__restrict__ cu, int B, int total, int C, int64_t xs,
-                   int64_t os, int n_l2, float eps, int *status) {
+                   int64_t os, int n_l2, float eps, int rows, int *status) {
     using V = Vec4<T>;
     constexpr int N = V::N;
     const int cv = blockIdx.y * CONV_THREADS + threadIdx.x;
@@ -110,7 +111,7 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
         int lo = 0, hi = B - 1;  // last s with base(s) <= y
         while (lo < hi) {
             int mid = (lo + hi + 1) >> 1;
-            if (conv_run_base(cu, mid) <= y) lo = mid; else hi = mid - 1;
+            if (conv_run_base(cu, mid, rows) <= y) lo = mid; else hi = mid - 1;
         }
         s = lo;
         sb = cu[s];
@@ -119,11 +120,11 @@ conv1d_silu_kernel(const uint64_t *__restrict__ state_ptrs, T *single_state,
             if (threadIdx.x == 0) raise_status(status, LA_DEV_BAD_SEQLENS);
             return;
         }
-        run = y - conv_run_base(cu, s);
+        run = y - conv_run_base(cu, s, rows);
     }
-    const int r0 = sb + run * CONV_ROWS;
+    const int r0 = sb + run * rows;
     if (run < 0 || r0 >= se) return;  // slot past this stream's runs (uniform per block)
-    const int r1 = min(r0 + CONV_ROWS, se);
+    const int r1 = min(r0 + rows, se);
 
     uint64_t wp[K][2], bp[2];
     load_taps<T, K>(w, bias, c0, active, wp, bp);
@@ -245,6 +246,22 @@ conv1d_silu_step_kernel(const uint64_t *__restrict__ state_ptrs, const T *__rest
     }
 }
 
+// Rows per run: longer runs read fewer halo rows and repeat less per-block setup, but make
+// fewer blocks. Take the longest of 256, 128 and 64 that still gives six waves of the resident
+// blocks (8 per SM); the small workloads keep 64.
+static int conv_rows(const ConvArgs &a, int col_blocks) {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+    const int64_t target = 6LL * 8 * sms;
+    for (int rows = 4 * CONV_ROWS; rows > CONV_ROWS; rows >>= 1) {
+        const int64_t slots = a.cu ? a.total / rows + a.B : (a.total + rows - 1) / rows;
+        if (slots * col_blocks >= target) return rows;
+    }
+    return CONV_ROWS;
+}
+
 template <typename T, int K, int HD>
 static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
     if (a.one_per_stream) {
@@ -257,14 +274,16 @@ static cudaError_t launch_conv_t(const ConvArgs &a, cudaStream_t st) {
     }
     constexpr int N = Vec4<T>::N;
     int nvec = a.channels / N;
-    // Run slots: single stream ceil(total/ROWS); varlen floor(total/ROWS) + B covers every
-    // stream's runs (stream s starts at slot floor(cu[s]/ROWS) + s).
-    int slots = a.cu ? a.total / CONV_ROWS + a.B : (a.total + CONV_ROWS - 1) / CONV_ROWS;
-    dim3 grid(slots, (nvec + CONV_THREADS - 1) / CONV_THREADS);
+    // Run slots: single stream ceil(total/rows); varlen floor(total/rows) + B covers every
+    // stream's runs (stream s starts at slot floor(cu[s]/rows) + s).
+    const int col_blocks = (nvec + CONV_THREADS - 1) / CONV_THREADS;
+    const int rows = conv_rows(a, col_blocks);
+    int slots = a.cu ? a.total / rows + a.B : (a.total + rows - 1) / rows;
+    dim3 grid(slots, col_blocks);
     conv1d_silu_kernel<T, K, HD><<<grid, CONV_THREADS, 0, st>>>(
         a.state_ptrs, (T *)a.single_state, (const T *)a.x, (const T *)a.w, (const T *)a.bias,
         (T *)a.out, a.cu, a.B, a.total, a.channels, a.x_stride, a.out_stride,
-        a.l2_heads * a.head_dim, a.eps, a.status);
+        a.l2_heads * a.head_dim, a.eps, rows, a.status);
     return cudaGetLastError();
 }
 
