@@ -9,9 +9,8 @@
 // GB300 design: the op is HBM-bound elementwise work, so each thread owns 4 channels (an 8-byte
 // bf16 / 16-byte fp32 vector) and a run of up to ROWS (64, 128 or 256: conv_rows) consecutive
 // tokens of ONE stream, keeping the kernel-1 previous rows in registers as a sliding window:
-// x is read once (plus
-// kernel-1 halo rows per run, served by L2) and out written once, with coalesced 16-byte
-// accesses. Runs are aligned to stream starts (stream s owns run slots floor(cu[s]/ROWS) + s
+// x is read once (plus kernel-1 halo rows per run, served by L2) and out written once, with
+// coalesced 16-byte accesses. Runs are aligned to stream starts (stream s owns run slots floor(cu[s]/ROWS) + s
 // onwards, found by binary search), so the first run of a stream is the only one that reads
 // its conv state, and that same thread advances the state in place afterwards: no race, no
 // second pass.
