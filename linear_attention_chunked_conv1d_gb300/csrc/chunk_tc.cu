@@ -1211,17 +1211,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
             // ---------------- o = scale (e^gc (Q H) + P U'): staged as bf16 [t][d] in shared
             //                  memory; written with 16-byte stores (rows < n) in the next chunk.
             //                  In the recurrence-only launch warp 0, held while the tensor core
-            //                  takes the state update, hands its 16 tokens to warp 12 (the same
-            //                  TMEM lane quadrant).
+            //                  takes the state update, hands its 16 tokens (GDN: 8 of them) to
+            //                  warp 12 (the same TMEM lane quadrant).
             {
                 __nv_bfloat16 *os = reinterpret_cast<__nv_bfloat16 *>(sm + SM_AT);
-                auto epi = [&](const int t0c) {
+                auto epi = [&](const int t0c, const int nt) {  // tokens t0c .. t0c + nt - 1 (16 or 8)
                     float vq[16], vp[16];
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
-                    tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
+                    if (nt == 16) {
+                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
+                        tc::tmem_ld16(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
+                    } else {
+                        tc::tmem_ld8(tc::tmem_addr(tm, lq, COL_D2 + 64 + t0c), vq);
+                        tc::tmem_ld8(tc::tmem_addr(tm, lq, COL_D4 + t0c), vp);
+                    }
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int ii = 0; ii < 16; ii += 2) {
+                        if (ii >= nt) break;
                         const int t = t0c + ii;
                         const float o0 = KDA ? vq[ii] + vp[ii] : fmaf(sf[SF_EG + t], vq[ii], vp[ii]);
                         const float o1 = KDA ? vq[ii + 1] + vp[ii + 1] : fmaf(sf[SF_EG + t + 1], vq[ii + 1], vp[ii + 1]);
@@ -1230,8 +1236,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) chunk_tc_kernel(const __grid_co
                         os[(t + 1) * O_LD + row] = pr.y;
                     }
                 };
-                if (FRONT || warp != 0) epi(C16 * part);
-                if (!FRONT && warp == 12) epi(0);
+                // GDN: warp 0 keeps 8 of its 16 tokens (warp 12, taking all 16, ended last)
+                if (FRONT || warp != 0) epi(C16 * part, 16);
+                if (!FRONT && !KDA && warp == 0) epi(0, 8);
+                if (!FRONT && warp == 12) epi(KDA ? 0 : 8, KDA ? 16 : 8);
                 pend_tok0 = tok0;
                 pend_n = n;
             }
